@@ -1,0 +1,349 @@
+"""Benchmark of the CSA2 decode step (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 1]
+
+A step is one pass of the whole hot path over one batch: append of the new
+token (main KV FP4, indexer key FP8, one FP8 window row per layer), the Full
+layer's indexer (scan, pool of 2,048 blocks, top-512), Reindex layers, Reuse
+layers, and every layer's sparse attention.  The default workload is the
+decode batch of 32 sequences at 65,536 tokens (one Full + three Reuse layers);
+the 1M-token, 20-layer batch of 4 is measured too and reported under
+"ctx_1m".  Inputs are seeded synthetic data; caches stay resident in HBM.
+
+Multi-GPU: sequences are independent, so each rank runs its own batch (weak
+scaling, no collective on the data path); value = all ranks' query-steps over
+the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode query-steps/s and achieved HBM GB/s (% of roofline) at 64K and 1M ctx"
+SCAN_BYTES_PER_POS = 68          # 64 FP8 key bytes + 4-byte scale per cached position
+FALLBACK_HBM_GBS = 6400.0
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.path = tempfile.mktemp(suffix=".csv")
+        self.proc = None
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-i", str(gpu_index), "-lms", "50"], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return float("nan")
+        sm = [num(r[1]) for r in rows]
+        mx = [num(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": reasons,
+                "samples": len(rows), "power_w_max": max(num(r[3]) for r in rows),
+                "window": "warm-up and timed steps"}
+
+
+# ------------------------------------------------------------------ distributed plumbing
+
+def dist_setup(n_gpus: int):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    import torch
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+
+
+# ------------------------------------------------------------------ our arm
+
+def kernels_per_step(wl) -> int:
+    from synth.workloads import REINDEX
+    n_re = sum(1 for m in wl.schedule if m == REINDEX)
+    return 1 + 5 + 2 * n_re + wl.n_layers          # append, Full select, Reindex, attention
+
+
+def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps: int = 100):
+    import torch
+    from sparse_attention_fp4_02_b300.runner import DecodeRunner
+    from synth.workloads import config
+
+    wl = config(cfg)
+    r = DecodeRunner(wl)
+    r.build_cache()
+    G = max(1, min(graph_steps, steps))
+    R = max(1, steps // G)
+    steps = R * G
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+    # one graph holding G steps; each step records its own events around the scan kernel
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        r.step()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    r.check_device_errors()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for i in range(G):
+            r.step(prof=ev[i])
+    g1 = r.capture()
+    for _ in range(max(1, math.ceil(warmup / G))):
+        g.replay()
+    barrier(world)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(R):
+        g.replay()
+    t1.record()
+    barrier(world)
+    ms = t0.elapsed_time(t1)
+    scan_ms = float(np.mean([a.elapsed_time(b) for a, b in ev]))
+    r.check_device_errors()
+    ms = max_over_ranks(ms, world)
+
+    # end to end through the public API with host buffers: pinned inputs in, outputs out, every step
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_in = [(pin(r.h_kv_new.view(np.int16)), r.kv_new), (pin(r.h_ik_new.view(np.int16)), r.ik_new),
+            (pin(r.h_swa_new.view(np.int16)), r.swa_new), (pin(r.h_q.view(np.int16)), r.q)]
+    h_in += [(pin(r.h_qidx[l].view(np.int16)), r.qidx[l]) for l in r.idx_layers]
+    h_in += [(pin(r.h_w[l]), r.w[l]) for l in r.idx_layers]
+    h_out = [torch.empty(r.out.shape, dtype=torch.float32).pin_memory(),
+             torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()]
+    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
+    d2h = sum(h.numel() * h.element_size() for h in h_out)
+    n_e2e = min(steps, 2000)
+
+    def e2e_step():
+        for h, d in h_in:
+            d.view(torch.int16 if d.dtype == torch.bfloat16 else d.dtype).copy_(h, non_blocking=True)
+        g1.replay()
+        h_out[0].copy_(r.out, non_blocking=True)
+        h_out[1].copy_(r.lse, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(n_e2e):
+        e2e_step()
+    e1.record()
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    r.check_device_errors()
+
+    q_steps = wl.B * steps * world
+    res = {
+        "wl": wl, "steps": steps, "ms": ms, "ms_per_step": ms / steps, "value": q_steps / (ms / 1e3),
+        "scan_ms": scan_ms, "scan_bytes": SCAN_BYTES_PER_POS * int(wl.lengths.sum()),
+        "e2e": {"value": wl.B * n_e2e * world / (e2e_ms / 1e3), "unit": "query-steps/s",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e},
+        "launches": kernels_per_step(wl) * steps,
+    }
+    del g, g1, r
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline(cfg: int, budget_s: float = 12.0):
+    """The oracle as it stands on this host: whole decode steps of a sample of sequences."""
+    from threadpoolctl import threadpool_info
+    from oracle import pipeline
+    from synth.workloads import config
+
+    wl = config(cfg)
+    n, spent = 0, 0.0
+    for b in range(wl.B):
+        st = pipeline.prepare(wl, b)
+        t = time.perf_counter()
+        pipeline.step(wl, b, st)
+        spent += time.perf_counter() - t
+        n += 1
+        if spent >= budget_s:
+            break
+    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    return {"value": n / spent, "unit": "query-steps/s", "cores": cores, "kind": "oracle",
+            "sample": f"{n} of {wl.B} sequences of {wl.name}, one full decode step each "
+                      f"({spent:.1f} s of CPU time; cache preparation excluded)"}
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    peak, peak_kind = peaks()
+    clock = ClockSampler(local)
+    res = measure_workload(args.config, args.steps, args.warmup, world)
+    res1m = None
+    if not args.no_1m and args.config != 2:
+        res1m = measure_workload(2, max(1, args.steps // 2), args.warmup, world)
+    clocks = clock.stop()
+    if rank != 0:
+        return
+    wl = res["wl"]
+    achieved = res["scan_bytes"] / (res["scan_ms"] / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": res["value"], "unit": "query-steps/s", "n_gpus": world,
+        "steps": res["steps"], "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp4-e2m1/fp8-e4m3 storage; f16 mma, f32 accumulate",
+        "data": "synthetic (seeded N(0,1) bf16 KV with 1% x8 outlier channels, U(0,1) head weights)",
+        "config": {"workload": wl.name, "batch": wl.B, "ctx": int(wl.lengths[0]), "layers": wl.schedule,
+                   "topk": wl.topk, "pool_blocks": wl.n_keep, "block": wl.block, "window": wl.window,
+                   "heads": wl.H, "l2": "inputs larger than L2 (scan streams "
+                                       f"{res['scan_bytes'] / 1e6:.1f} MB per step)",
+                   "parallelism": f"replicas x{world} (one batch per GPU)"},
+        "roofline": {"bound": "hbm", "kernel": "indexer scan", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": None, "scan_us": res["scan_ms"] * 1e3,
+                     "algorithmic_bytes": res["scan_bytes"],
+                     "step_frac": (res["scan_bytes"] + 68096 * wl.B * wl.n_layers) / (res["ms_per_step"] / 1e3)
+                     / 1e9 / peak},
+        "e2e": {k: v for k, v in res["e2e"].items() if k != "steps"},
+        "gpu_launches": res["launches"],
+        "clocks": clocks,
+    }
+    if res1m:
+        w2 = res1m["wl"]
+        a2 = res1m["scan_bytes"] / (res1m["scan_ms"] / 1e3) / 1e9
+        line["ctx_1m"] = {"workload": w2.name, "value": res1m["value"], "unit": "query-steps/s",
+                          "ms_per_step": res1m["ms_per_step"], "steps": res1m["steps"],
+                          "scan_us": res1m["scan_ms"] * 1e3, "scan_gbs": a2, "scan_frac": a2 / peak,
+                          "e2e": res1m["e2e"]["value"], "gpu_launches": res1m["launches"]}
+    if not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(args.config)
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm (the CPU oracle)
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    from threadpoolctl import threadpool_info
+    from oracle import pipeline
+    from synth.workloads import config
+
+    wl = config(args.config)
+    # each step: one sequence's whole decode step (a bounded sample of the batch)
+    n_prep = max(1, min(wl.B, 4))
+    states = [pipeline.prepare(wl, b) for b in range(n_prep)]
+    for i in range(args.warmup):
+        pipeline.step(wl, i % n_prep, states[i % n_prep])
+    t = time.perf_counter()
+    for i in range(args.steps):
+        pipeline.step(wl, i % n_prep, states[i % n_prep])
+    dt = time.perf_counter() - t
+    value = args.steps / dt
+    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "query-steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": wl.name, "batch": wl.B, "ctx": int(wl.lengths[0]), "layers": wl.schedule},
+        "cpu_baseline": {"value": value, "unit": "query-steps/s", "cores": cores, "kind": "oracle",
+                         "sample": f"each step is one sequence of {wl.name} (of {wl.B}) through every layer"},
+        "e2e": {"value": value, "unit": "query-steps/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 4])
+    ap.add_argument("--no-1m", action="store_true", help="skip the 1M-context workload")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
+        run_reference(args, world, rank)
+        return
+    world, rank, local = dist_setup(args.gpus)
+    run_ours(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

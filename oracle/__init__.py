@@ -27,4 +27,4 @@ conversion, scaled_dot_product_attention) and brute force.  The page-level
 byte budget (890 B/token) is not reproducible at these dimensions: parity
 unpinned for that figure, and nothing here computes it.
 """
-from . import formats, append, indexer, attention, bruteforce  # noqa: F401
+from . import formats, append, indexer, attention, bruteforce, pipeline  # noqa: F401

@@ -1,0 +1,60 @@
+// Internal launchers of the CSA2 library (host side).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "csa2.h"
+
+namespace csa2 {
+
+cudaError_t launch_append(const csa2_cache &c, const csa2_swa *swa, int n_swa, const uint16_t *kv_new,
+                          const uint16_t *ik_new, const uint16_t *swa_new, const float *cos,
+                          const float *sin, int64_t rope_len, const int32_t *seq_id, const int64_t *pos,
+                          int64_t n, int32_t *d_err, cudaStream_t st);
+cudaError_t launch_test_fp4(const float *x, int64_t n_groups, uint8_t *codes, uint8_t *scales,
+                            cudaStream_t st);
+cudaError_t launch_test_fp8(const float *x, int64_t n, int C, uint8_t *codes, float *scale, cudaStream_t st);
+
+// ---- indexer ----
+struct IndexerWs {           // carved out of the caller's workspace
+  uint32_t *hist;            // [B][4096]
+  uint32_t *smax;            // [B]   scan's max key scale (float bits)
+  uint32_t *smax2;           // [B]   position stage's max key scale
+  uint32_t *cand_cnt;        // [B]
+  uint32_t *pcb_cnt;         // [B]
+  float *bmax;               // [B][nbm]
+  uint64_t *cand;            // [B][nbm]
+  int32_t *pcb;              // [B][n_keep]
+  float *pvals;              // [B][n_keep * block]
+  int32_t *unc_id;           // [B][unc_cap]
+  double *unc_val;           // [B][unc_cap]
+  int64_t nbm, unc_cap;
+  size_t zero_bytes;         // bytes at the start that must be zeroed per call
+};
+
+size_t indexer_ws_bytes(int32_t B, int64_t max_len, int32_t block, int32_t n_keep);
+IndexerWs indexer_ws_carve(void *ws, int32_t B, int64_t max_len, int32_t block, int32_t n_keep);
+
+cudaError_t launch_full_select(const csa2_cache &c, const uint16_t *q, const float *w, int block,
+                               int n_keep, int topk, int64_t max_len, int32_t *pool, int32_t *topk_idx,
+                               const IndexerWs &ws, int32_t *d_err, const csa2_profile *prof,
+                               cudaStream_t st);
+cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const float *w,
+                                  const int32_t *pool, int block, int n_keep, int topk, int64_t max_len,
+                                  int32_t *topk_idx, const IndexerWs &ws, int32_t *d_err, cudaStream_t st);
+cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len,
+                               float *sigma, double *bound, const IndexerWs &ws, int32_t *d_err,
+                               cudaStream_t st);
+
+// ---- attention ----
+size_t attn_ws_bytes(int64_t T, int32_t H, int32_t topk, int32_t window);
+cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const uint16_t *q, int H, int64_t T,
+                               const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx,
+                               int topk, int window, float tau, float *out, float *lse, void *ws,
+                               int32_t *d_err, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace csa2

@@ -1,0 +1,171 @@
+"""Decoder layer-pattern runner over the C ABI.
+
+A decode step of the CSA2 decoder (origotech.dev deep dive, subsection
+"Compressed Sparse Attention 2(CSA2)"): the new token's KV is quantised and
+appended, the first Full layer's indexer scores every cached position and
+keeps a 2,048-block pool plus its top-512, every Reindex layer rescores the
+pool with its own indexer queries, every Reuse layer passes the indices on,
+and every layer runs sparse attention over its indices plus its own
+128-token FP8 window.
+
+All compute happens in libcsa2.so; this module allocates device memory with
+torch, fills caches from seeded synthetic inputs and sequences the calls
+(optionally captured into one CUDA graph).
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+import synth
+from synth.workloads import FULL, REINDEX, REUSE, DecodeWorkload
+
+from . import (Cache, SwaRing, OP_ATTN_DECODE, OP_FULL_SELECT, alloc_workspace, indexer_full_select,
+               indexer_reindex_select, kv_append_fp4, sparse_attn_decode, workspace_bytes)
+
+
+def _to_dev(a: np.ndarray, dtype, device):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(device=device, dtype=dtype)
+
+
+def _bf16_dev(bits: np.ndarray, device):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+class DecodeRunner:
+    """Caches, per-step inputs and outputs of one decode workload on one GPU."""
+
+    def __init__(self, wl: DecodeWorkload, device="cuda", rope_len: int | None = None):
+        self.wl = wl
+        self.device = device
+        B = wl.B
+        L = wl.lengths.astype(np.int64)
+        self.lengths = L
+        self.max_len = int(L.max())
+        base = np.zeros(B, dtype=np.int64)
+        base[1:] = np.cumsum(((L + 15) // 16) * 16)[:-1]
+        self.seq_base_np = base
+        self.T_cap = int(base[-1] + ((L[-1] + 15) // 16) * 16)
+        self.cache = Cache(self.T_cap, B, device)
+        self.cache.seq_base.copy_(torch.from_numpy(base))
+        self.cache.seq_len.copy_(torch.from_numpy(L.astype(np.int32)))
+        self.swa = [SwaRing(B, wl.ring, device) for _ in range(wl.n_layers)]
+        cos, sin = synth.rope_table(rope_len or self.max_len)
+        self.rope_cos = torch.from_numpy(cos).to(device)
+        self.rope_sin = torch.from_numpy(sin).to(device)
+        self.d_err = torch.zeros(1, dtype=torch.int32, device=device)
+        self.kv_outliers = synth.outlier_channels(wl.seed, synth.Stream.KV_OUTLIER)
+        self.swa_outliers = synth.outlier_channels(wl.seed, synth.Stream.SWA_OUTLIER)
+        self._make_step_inputs()
+        self._make_outputs()
+
+    # ------------------------------------------------------------------ inputs
+    def _make_step_inputs(self):
+        wl, dev, B = self.wl, self.device, self.wl.B
+        s = wl.seed
+        newpos = self.lengths - 1
+        rows_new = synth.row_id(np.arange(B), newpos)
+        self.h_kv_new = synth.normals_bf16(s, synth.Stream.KV, 0, rows_new, 128, self.kv_outliers)
+        self.h_ik_new = synth.normals_bf16(s, synth.Stream.IK, 0, rows_new, 64)
+        self.h_swa_new = np.stack([synth.normals_bf16(s, synth.Stream.SWA, l, rows_new, 128, self.swa_outliers)
+                                   for l in range(wl.n_layers)])
+        self.h_seq_id = np.arange(B, dtype=np.int32)
+        self.h_pos = newpos.astype(np.int64)
+        self.h_q = np.stack([synth.normals_bf16(s, synth.Stream.Q, l,
+                                                synth.row_id(np.repeat(np.arange(B), wl.H), np.tile(np.arange(wl.H), B)),
+                                                128).reshape(B, wl.H, 128) for l in range(wl.n_layers)])
+        self.idx_layers = [l for l, m in enumerate(wl.schedule) if m in (FULL, REINDEX)]
+        self.h_qidx = {l: synth.normals_bf16(s, synth.Stream.QIDX, l,
+                                             synth.row_id(np.repeat(np.arange(B), 8), np.tile(np.arange(8), B)),
+                                             64).reshape(B, 8, 64) for l in self.idx_layers}
+        self.h_w = {l: np.stack([synth.head_weights(s, l, b) for b in range(B)]) for l in self.idx_layers}
+        # device copies
+        self.kv_new = _bf16_dev(self.h_kv_new, dev)
+        self.ik_new = _bf16_dev(self.h_ik_new, dev)
+        self.swa_new = _bf16_dev(self.h_swa_new, dev)
+        self.seq_id = _to_dev(self.h_seq_id, torch.int32, dev)
+        self.pos = _to_dev(self.h_pos, torch.int64, dev)
+        self.q = _bf16_dev(self.h_q, dev)
+        self.qidx = {l: _bf16_dev(v, dev) for l, v in self.h_qidx.items()}
+        self.w = {l: _to_dev(v, torch.float32, dev) for l, v in self.h_w.items()}
+
+    def _make_outputs(self):
+        wl, dev, B = self.wl, self.device, self.wl.B
+        self.pool = torch.full((B, wl.n_keep), -1, dtype=torch.int32, device=dev)
+        self.topk = {l: torch.full((B, wl.topk), -1, dtype=torch.int32, device=dev) for l in self.idx_layers}
+        self.out = torch.zeros((wl.n_layers, B, wl.H, 128), dtype=torch.float32, device=dev)
+        self.lse = torch.zeros((wl.n_layers, B, wl.H), dtype=torch.float32, device=dev)
+        self.ws_idx = alloc_workspace(workspace_bytes(OP_FULL_SELECT, B, self.max_len, wl.block, wl.n_keep, wl.topk),
+                                      dev)
+        self.ws_attn = alloc_workspace(workspace_bytes(OP_ATTN_DECODE, T=B, H=wl.H, topk=wl.topk, window=wl.window),
+                                       dev)
+        self.tau = 1.0 / math.sqrt(128.0)
+
+    def layer_topk(self, layer: int):
+        """The index buffer layer ``layer`` attends over (Reuse layers share the previous one)."""
+        src = max(l for l in self.idx_layers if l <= layer)
+        return self.topk[src]
+
+    # ------------------------------------------------------------------ cache build
+    def build_cache(self, chunk: int = 1 << 18):
+        """Append positions 0..L-2 of every sequence (the step appends L-1) and the window rows."""
+        wl, dev, s = self.wl, self.device, self.wl.seed
+        for b in range(wl.B):
+            n_old = int(self.lengths[b]) - 1
+            for lo in range(0, n_old, chunk):
+                hi = min(n_old, lo + chunk)
+                pos = np.arange(lo, hi, dtype=np.int64)
+                rows = synth.row_id(b, pos)
+                kv = _bf16_dev(synth.normals_bf16(s, synth.Stream.KV, 0, rows, 128, self.kv_outliers), dev)
+                ik = _bf16_dev(synth.normals_bf16(s, synth.Stream.IK, 0, rows, 64), dev)
+                sid = torch.full((hi - lo,), b, dtype=torch.int32, device=dev)
+                kv_append_fp4(self.cache, None, kv, ik, None, self.rope_cos, self.rope_sin, sid,
+                              torch.from_numpy(pos).to(dev), self.d_err)
+            # window rows before the new token, every layer
+            lo = max(0, n_old - (wl.window - 1))
+            if n_old > lo:
+                pos = np.arange(lo, n_old, dtype=np.int64)
+                rows = synth.row_id(b, pos)
+                kv = _bf16_dev(synth.normals_bf16(s, synth.Stream.KV, 0, rows, 128, self.kv_outliers), dev)
+                sw = _bf16_dev(np.stack([synth.normals_bf16(s, synth.Stream.SWA, l, rows, 128, self.swa_outliers)
+                                         for l in range(wl.n_layers)]), dev)
+                sid = torch.full((n_old - lo,), b, dtype=torch.int32, device=dev)
+                kv_append_fp4(self.cache, self.swa, kv, None, sw, self.rope_cos, self.rope_sin, sid,
+                              torch.from_numpy(pos).to(dev), self.d_err)
+        torch.cuda.synchronize()
+
+    # ------------------------------------------------------------------ the step
+    def step(self, prof=None):
+        """One decode step through every layer of the schedule."""
+        wl = self.wl
+        kv_append_fp4(self.cache, self.swa, self.kv_new, self.ik_new, self.swa_new, self.rope_cos, self.rope_sin,
+                      self.seq_id, self.pos, self.d_err)
+        for l, mode in enumerate(wl.schedule):
+            if mode == FULL:
+                indexer_full_select(self.cache, self.qidx[l], self.w[l], wl.block, wl.n_keep, wl.topk, self.max_len,
+                                    self.pool, self.topk[l], self.ws_idx, self.d_err, prof=prof)
+            elif mode == REINDEX:
+                indexer_reindex_select(self.cache, self.qidx[l], self.w[l], self.pool, wl.block, wl.n_keep, wl.topk,
+                                       self.max_len, self.topk[l], self.ws_idx, self.d_err)
+            sparse_attn_decode(self.cache, self.swa[l], self.q[l], self.seq_id, self.pos, self.layer_topk(l),
+                               wl.window, self.tau, self.out[l], self.lse[l], self.ws_attn, self.d_err)
+
+    def check_device_errors(self):
+        v = int(self.d_err.item())
+        if v:
+            raise RuntimeError(f"device error bits 0x{v:x}")
+
+    def capture(self, prof=None):
+        """Capture one step into a CUDA graph; returns the graph (replay with .replay())."""
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(s):
+            self.step(prof)           # warm-up outside capture
+        torch.cuda.current_stream().wait_stream(s)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(prof)
+        return g
