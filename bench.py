@@ -111,13 +111,20 @@ def dist_setup(n_gpus: int):
 
 
 def max_over_ranks(x: float, world: int) -> float:
+    """The largest of every rank's x (the slowest rank's time)."""
     if world == 1:
         return x
     import torch
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def aggregate_rate(units_per_rank: int, world: int, ms_max: float) -> float:
+    """Whole-job throughput: the units all ranks processed over the slowest rank's time."""
+    return units_per_rank * world / (ms_max / 1e3)
 
 
 def barrier(world: int):
@@ -125,7 +132,8 @@ def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
         dist.barrier()
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()
 
 
 # ------------------------------------------------------------------ our arm
@@ -148,6 +156,9 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
     R = max(1, steps // G)
     steps = R * G
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(G)]
+    for a, b in ev:          # torch creates the CUDA event on first record; the library needs the handle
+        a.record()
+        b.record()
     # one graph holding G steps; each step records its own events around the scan kernel
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -206,11 +217,10 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     r.check_device_errors()
 
-    q_steps = wl.B * steps * world
     res = {
-        "wl": wl, "steps": steps, "ms": ms, "ms_per_step": ms / steps, "value": q_steps / (ms / 1e3),
+        "wl": wl, "steps": steps, "ms": ms, "ms_per_step": ms / steps, "value": aggregate_rate(wl.B * steps, world, ms),
         "scan_ms": scan_ms, "scan_bytes": SCAN_BYTES_PER_POS * int(wl.lengths.sum()),
-        "e2e": {"value": wl.B * n_e2e * world / (e2e_ms / 1e3), "unit": "query-steps/s",
+        "e2e": {"value": aggregate_rate(wl.B * n_e2e, world, e2e_ms), "unit": "query-steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e},
         "launches": kernels_per_step(wl) * steps,
     }
@@ -219,9 +229,20 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
     return res
 
 
+def blas_threads() -> int:
+    """Threads the oracle's numpy/BLAS calls use on this host."""
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    except ImportError:
+        for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+            if os.environ.get(var, "").isdigit():
+                return int(os.environ[var])
+        return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
 def cpu_baseline(cfg: int, budget_s: float = 12.0):
     """The oracle as it stands on this host: whole decode steps of a sample of sequences."""
-    from threadpoolctl import threadpool_info
     from oracle import pipeline
     from synth.workloads import config
 
@@ -235,7 +256,7 @@ def cpu_baseline(cfg: int, budget_s: float = 12.0):
         n += 1
         if spent >= budget_s:
             break
-    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    cores = blas_threads()
     return {"value": n / spent, "unit": "query-steps/s", "cores": cores, "kind": "oracle",
             "sample": f"{n} of {wl.B} sequences of {wl.name}, one full decode step each "
                       f"({spent:.1f} s of CPU time; cache preparation excluded)"}
@@ -292,7 +313,6 @@ def run_ours(args, world, rank, local):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    from threadpoolctl import threadpool_info
     from oracle import pipeline
     from synth.workloads import config
 
@@ -307,7 +327,7 @@ def run_reference(args, world, rank):
         pipeline.step(wl, i % n_prep, states[i % n_prep])
     dt = time.perf_counter() - t
     value = args.steps / dt
-    cores = max([i.get("num_threads", 1) for i in threadpool_info()] + [1])
+    cores = blas_threads()
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "query-steps/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt / args.steps * 1e3,

@@ -205,12 +205,12 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
  * (ttj.kr article, section "CSA2와 어텐션 재설계"; origotech.dev deep dive,
  * subsection "Compressed Sparse Attention 2(CSA2)")
  *   swa            this layer's window ring (host struct)
- *   q              bf16 [T][H][128]; H a multiple of 16, <= 128
+ *   q              bf16 [T][H][128] (16-byte aligned); H a multiple of 16, <= 128
  *   q_seq, q_pos   int32 [T], int64 [T]: sequence and position of each query row
  *   topk_idx       int32 [T][topk] positions (<= q_pos), -1 entries skipped
  *   window         window length W (0..1024, <= swa->ring)
  *   softmax_scale  tau (use 1/sqrt(128))
- *   out            float [T][H][128] = sum_j softmax(z)_j * v_j, z_j = tau * q . k_j
+ *   out            float [T][H][128] (16-byte aligned) = sum_j softmax(z)_j * v_j, z_j = tau * q . k_j
  *   lse            float [T][H] = log sum_j exp(z_j), or NULL
  * One softmax spans the valid selected rows (FP4, dequantised exactly) and
  * the window rows max(0, p-W+1)..p (FP8 value times the row's scale); V = K.
@@ -220,6 +220,7 @@ int sparse_attn_decode(const csa2_cache *cache, const csa2_swa *swa, const uint1
                        int64_t T, const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx,
                        int32_t topk, int32_t window, float softmax_scale, float *out, float *lse,
                        void *ws, size_t ws_bytes, int32_t *d_err, csa2_stream_t stream);
+/* (sparse_attn_decode needs no workspace: ws may be NULL and ws_bytes 0.) */
 
 /* ---- test-only exports (same device code as the entry points above) ---- */
 

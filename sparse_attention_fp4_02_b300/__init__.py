@@ -19,7 +19,8 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libcsa2.so")
+# CSA2_LIB selects another build of the library (same ABI); default: the in-tree build
+LIB_PATH = os.environ.get("CSA2_LIB") or os.path.join(_HERE, "libcsa2.so")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_attention_fp4_02_b300.build`")

@@ -99,4 +99,15 @@ __device__ __forceinline__ uint4 ld_nc16(const void *p) {
   return __ldg(reinterpret_cast<const uint4 *>(p));
 }
 
+// cp.async copies into shared memory; pred false zero-fills without reading the source
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src, bool pred) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(pred ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void *src, bool pred) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src), "r"(pred ? 4 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+
 }  // namespace csa2

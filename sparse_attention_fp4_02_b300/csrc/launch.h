@@ -29,7 +29,7 @@ struct IndexerWs {           // carved out of the caller's workspace
   int32_t *pcb;              // [B][n_keep]
   float *pvals;              // [B][n_keep * block]
   int32_t *unc_id;           // [B][unc_cap]
-  double *unc_val;           // [B][unc_cap]
+  float2 *unc_val;           // [B][unc_cap] exact scores as normalised double-floats
   int64_t nbm, unc_cap;
   size_t zero_bytes;         // bytes at the start that must be zeroed per call
 };

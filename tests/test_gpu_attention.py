@@ -143,7 +143,12 @@ def test_permuted_and_padded_indices_give_the_same_output():
     shuffled = np.concatenate([topk[:, rng.permutation(512)], np.full((1, 64), -1, np.int32)], axis=1)
     shuffled = shuffled[:, rng.permutation(576)]
     out2, lse2, _ = w.run(q, np.zeros(1, np.int32), q_pos, shuffled, 128)
-    assert np.allclose(out1, out2, rtol=1e-5, atol=1e-6) and np.allclose(lse1, lse2, atol=1e-5)
+    # Only the summation order changes: f32 accumulation over <= 640 rows plus the f16 hi/lo split
+    # of P (~2^-22 relative) moves an output by far less than 3e-5 of its row's largest value,
+    # while a dropped or doubled row moves it by ~1e-3 (one of 640 weights).
+    e = attn_rel_err(out2, out1)
+    print(f"permutation rel diff {e:.3e}")
+    assert e < 3e-5 and np.allclose(lse1, lse2, atol=1e-5)
 
 
 def test_non_causal_index_is_flagged_and_skipped():
