@@ -201,6 +201,37 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
                            size_t ws_bytes, int32_t *d_err, csa2_stream_t stream);
 
 /*
+ * indexer_reindex_select_static - indexer_reindex_select for callers that
+ * cannot allocate device memory.  The paper has no counterpart: this is a
+ * calling convention, not a step of the method.
+ *
+ * Some callers have no way to obtain a workspace: a plugin inside an engine
+ * whose memory planner owns every byte of the device and forbids cudaMalloc,
+ * or code on a latency-critical path where cudaMalloc/cudaFree would
+ * synchronise the device.  This entry point takes the same arguments as
+ * indexer_reindex_select minus ws/ws_bytes, gives the same result, and
+ * allocates nothing: its scratch is one static device array of
+ * CSA2_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads
+ * the library holds until the process exits.
+ *   Limit: the call needs 4*B*(4100 + n_keep_blocks*(1 + 4*block)) bytes of
+ *   scratch (each of its 9 arrays rounded up to 256 bytes); every call with
+ *   B*n_keep_blocks*block <= 524,288 and B <= 64 fits.  A larger call returns CSA2_ERR_WORKSPACE and
+ *   launches nothing.
+ *   Set-up: the first call on each device resolves the array's device address
+ *   with that device current; make that first call before any stream capture.
+ *   Sharing: every call uses the same array and leaves its contents behind
+ *   (the call clears what must start at zero).  Calls whose kernels overlap
+ *   on the GPU (different streams, or several host threads) race on it:
+ *   serialise them, for example on one stream.
+ * Status codes, device error bits and output layout are indexer_reindex_select's.
+ */
+#define CSA2_STATIC_SCRATCH_BYTES (12u << 20)
+int indexer_reindex_select_static(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
+                                  const int32_t *pool_blocks, int32_t block, int32_t n_keep_blocks,
+                                  int32_t topk, int64_t max_len, int32_t *topk_idx, int32_t *d_err,
+                                  csa2_stream_t stream);
+
+/*
  * sparse_attn_decode - gathered FP4 dequantisation fused into sparse attention.
  * (ttj.kr article, section "CSA2와 어텐션 재설계"; origotech.dev deep dive,
  * subsection "Compressed Sparse Attention 2(CSA2)")

@@ -23,7 +23,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.environ.get("CSA2_LIB") or os.path.join(_HERE, "libcsa2.so")
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"{LIB_PATH} is missing: build it with `python -m sparse_attention_fp4_02_b300.build`")
+    raise ImportError(f"{LIB_PATH} is missing: build it with `python sparse_attention_fp4_02_b300/build.py`")
 _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID_ARG, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
@@ -65,6 +65,7 @@ _ws_bytes = _sig("csa2_workspace_bytes", [ctypes.c_int, _I32, _I64, _I32, _I32, 
 _append = _sig("kv_append_fp4", [_P, _P, _I32, _P, _P, _P, _P, _P, _I64, _P, _P, _I64, _P, _P])
 _full = _sig("indexer_full_select", [_P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P, _SZ, _P, _P, _P])
 _reindex = _sig("indexer_reindex_select", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _SZ, _P, _P])
+_reindex_static = _sig("indexer_reindex_select_static", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P])
 _attn = _sig("sparse_attn_decode", [_P, _P, _P, _I32, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P, _P, _SZ,
                                     _P, _P])
 _t_fp4 = _sig("csa2_test_quantize_fp4", [_P, _I64, _P, _P, _P])
@@ -72,7 +73,7 @@ _t_fp8 = _sig("csa2_test_quantize_fp8", [_P, _I64, _I32, _P, _P, _P])
 _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _P, _P])
 
 EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "indexer_full_select",
-            "indexer_reindex_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
+            "indexer_reindex_select", "indexer_reindex_select_static", "sparse_attn_decode", "csa2_test_quantize_fp4",
             "csa2_test_quantize_fp8", "csa2_test_index_scores")
 
 
@@ -168,6 +169,14 @@ def indexer_reindex_select(cache: Cache, q_idx, w, pool_blocks, block, n_keep_bl
     _check(_reindex(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(pool_blocks), block, n_keep_blocks,
                     topk, int(max_len), _ptr(topk_idx), _ptr(ws), ws.numel(), _ptr(d_err), _stream(stream)),
            "indexer_reindex_select")
+
+
+def indexer_reindex_select_static(cache: Cache, q_idx, w, pool_blocks, block, n_keep_blocks, topk, max_len,
+                                  topk_idx, d_err, stream=None):
+    """indexer_reindex_select without a workspace (scratch is a static array in the library)."""
+    _check(_reindex_static(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(pool_blocks), block,
+                           n_keep_blocks, topk, int(max_len), _ptr(topk_idx), _ptr(d_err), _stream(stream)),
+           "indexer_reindex_select_static")
 
 
 def sparse_attn_decode(cache: Cache, swa: SwaRing, q, q_seq, q_pos, topk_idx, window, softmax_scale, out, lse, ws,

@@ -1,6 +1,7 @@
 // C ABI of the CSA2 library: host-side validation, workspace sizing, dispatch.
 #include <cstdint>
 #include <cstring>
+#include <mutex>
 
 #include "common.cuh"
 #include "launch.h"
@@ -163,6 +164,56 @@ int sparse_attn_decode(const csa2_cache *cache, const csa2_swa *swa, const uint1
   if (window == 0) { sw.ring = 1; }
   return cuda_status(launch_attn_decode(*cache, sw, q, H, T, q_seq, q_pos, topk_idx, topk, window, softmax_scale,
                                         out, lse, ws, d_err, (cudaStream_t)stream));
+}
+
+}  // extern "C"
+
+// ---- workspace-free Reindex: scratch in a static device array ----------------------
+namespace {
+
+// Scratch of indexer_reindex_select_static.  In host code this name is only a handle
+// for cudaGetSymbolAddress, never a device address.
+__device__ __align__(256) unsigned char g_reindex_scratch[CSA2_STATIC_SCRATCH_BYTES];
+
+// The array's device address on the current device, resolved once per device.
+int static_scratch(void **out) {
+  static std::mutex mu;
+  static void *addr[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
+  if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_reindex_scratch) != cudaSuccess || !p) return CSA2_ERR_CUDA;
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return CSA2_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int indexer_reindex_select_static(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
+                                  const int32_t *pool_blocks, int32_t block, int32_t n_keep_blocks, int32_t topk,
+                                  int64_t max_len, int32_t *topk_idx, int32_t *d_err, csa2_stream_t stream) {
+  if (!cache_ok(cache) || !q_idx || !aligned(q_idx, 16) || !w || !aligned(w, 4) || !pool_blocks || !topk_idx ||
+      !d_err)
+    return CSA2_ERR_INVALID_ARG;
+  if (!select_sizes_ok(cache->B, max_len, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
+  // a Reindex call touches no per-block arrays, so its layout is the one for max_len 0
+  if (indexer_ws_bytes(cache->B, 0, block, n_keep_blocks) > (size_t)CSA2_STATIC_SCRATCH_BYTES)
+    return CSA2_ERR_WORKSPACE;
+  int st = device_ok();
+  if (st != CSA2_OK) return st;
+  void *scratch = nullptr;
+  st = static_scratch(&scratch);
+  if (st != CSA2_OK) return st;
+  IndexerWs iw = indexer_ws_carve(scratch, cache->B, 0, block, n_keep_blocks);
+  return cuda_status(launch_reindex_select(*cache, q_idx, w, pool_blocks, block, n_keep_blocks, topk, max_len,
+                                           topk_idx, iw, d_err, (cudaStream_t)stream));
 }
 
 int csa2_test_quantize_fp4(const float *x, int64_t n_groups, uint8_t *codes, uint8_t *scales, csa2_stream_t stream) {
