@@ -1,7 +1,8 @@
 """Build the CSA2 C-ABI library in-tree: sparse_attention_fp4_02_b300/libcsa2.so.
 
-nvcc cross-compiles for sm_103a on a machine without a GPU.  Usage:
-    python -m sparse_attention_fp4_02_b300.build [--verbose]
+nvcc cross-compiles for sm_103a on a machine without a GPU.  Usage (run it as a
+script: importing the package loads the library this builds):
+    python sparse_attention_fp4_02_b300/build.py [--verbose]
 """
 from __future__ import annotations
 

@@ -9,8 +9,11 @@ if ROOT not in sys.path:
 def _ensure_library():
     lib = os.path.join(ROOT, "sparse_attention_fp4_02_b300", "libcsa2.so")
     if not os.path.exists(lib):
-        from sparse_attention_fp4_02_b300.build import build
-        build()
+        import importlib.util     # load the build script by path: the package imports the library
+        spec = importlib.util.spec_from_file_location("_csa2_build", os.path.join(os.path.dirname(lib), "build.py"))
+        mod = importlib.util.module_from_spec(spec)
+        spec.loader.exec_module(mod)
+        mod.build()
 
 
 _ensure_library()
