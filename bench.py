@@ -141,7 +141,9 @@ def barrier(world: int):
 def kernels_per_step(wl) -> int:
     from synth.workloads import REINDEX
     n_re = sum(1 for m in wl.schedule if m == REINDEX)
-    return 1 + 5 + 2 * n_re + wl.n_layers          # append, Full select, Reindex, attention
+    n_blocks = -(-int(wl.lengths.max()) // wl.block)
+    full = 4 if n_blocks <= 16384 else 5            # scan, [collect,] finalize, score, select
+    return 1 + full + 2 * n_re + wl.n_layers        # append, Full select, Reindex, attention
 
 
 def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps: int = 100):

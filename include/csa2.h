@@ -178,7 +178,7 @@ int kv_append_fp4(const csa2_cache *cache, const csa2_swa *swa_layers, int32_t n
  *                  (score desc, position asc), ascending, -1 padded
  * Ranking is exact: approximate tensor-core scores carry a rigorous error
  * bound, and every item whose bound straddles a selection threshold is
- * rescored exactly in float64 before the final choice.
+ * rescored exactly (64-bit integer dot products) before the final choice.
  */
 int indexer_full_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
                         int32_t block, int32_t n_keep_blocks, int32_t topk, int64_t max_len,
@@ -213,7 +213,7 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
  * allocates nothing: its scratch is one static device array of
  * CSA2_STATIC_SCRATCH_BYTES inside the library, which every GPU that loads
  * the library holds until the process exits.
- *   Limit: the call needs 4*B*(4100 + n_keep_blocks*(1 + 4*block)) bytes of
+ *   Limit: the call needs 4*B*(8196 + n_keep_blocks*(1 + 6*block)) bytes of
  *   scratch (each of its 9 arrays rounded up to 256 bytes); every call with
  *   B*n_keep_blocks*block <= 524,288 and B <= 64 fits.  A larger call returns CSA2_ERR_WORKSPACE and
  *   launches nothing.
@@ -225,7 +225,7 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
  *   serialise them, for example on one stream.
  * Status codes, device error bits and output layout are indexer_reindex_select's.
  */
-#define CSA2_STATIC_SCRATCH_BYTES (12u << 20)
+#define CSA2_STATIC_SCRATCH_BYTES (16u << 20)
 int indexer_reindex_select_static(const csa2_cache *cache, const uint16_t *q_idx, const float *w,
                                   const int32_t *pool_blocks, int32_t block, int32_t n_keep_blocks,
                                   int32_t topk, int64_t max_len, int32_t *topk_idx, int32_t *d_err,

@@ -28,9 +28,9 @@
 
 namespace csa2 {
 
-constexpr double kEpsAcc = 1.52587890625e-05;        // 2^-16
-constexpr double kConvAbs = 64.0 * 2.98023223876953125e-08;  // 64 * 2^-25
-constexpr double kRel = 1.9073486328125e-06;          // 2^-19
+constexpr float kEpsAcc448 = 448.0f * 0x1p-16f;      // 448 * 2^-16 (accumulation, relative to sum |terms|)
+constexpr float kConvAbs448 = 448.0f * 64.0f * 0x1p-25f;   // 448 * 64 * 2^-25 (queries below the f16 range)
+constexpr float kRelF = 0x1p-19f;                     // r = 2^-19
 constexpr int kMaxSel = 4096;                          // n_keep_blocks limit
 
 // ------------------------------------------------------------------ query fragments
@@ -83,31 +83,35 @@ __device__ __forceinline__ void load_qfrag(const uint16_t *q_seq, const float *w
   f.wi1 = __ldg(w_seq + 2 * t + 1) * pow2f(-c1);
 }
 
-// Absolute error bound E of one sequence (identical in every lane).
-__device__ double seq_bound(const uint16_t *q_seq, const float *w_seq, float smax, int lane) {
+// Absolute error bound E of one sequence (identical in every lane), rounded upward at
+// every step so that the float result is never below the exact bound.
+__device__ float seq_bound(const uint16_t *q_seq, const float *w_seq, float smax, int lane) {
   float v[16];
   const int c = load_q16(q_seq, lane, v);
   const float sc = pow2f(c);
-  double l1 = 0.0;
+  float l1 = 0.f;
 #pragma unroll
-  for (int i = 0; i < 16; ++i) l1 += fabs((double)__half2float(__float2half_rn(v[i] * sc)));
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  for (int i = 0; i < 16; ++i) l1 = __fadd_ru(l1, fabsf(__half2float(__float2half_rn(v[i] * sc))));
+  l1 = __fadd_ru(l1, __shfl_xor_sync(0xffffffffu, l1, 1));
+  l1 = __fadd_ru(l1, __shfl_xor_sync(0xffffffffu, l1, 2));
   const int g = lane >> 2;
-  double term = 0.0;
+  float term = 0.f;
   if ((lane & 3) == 0)
-    term = (double)__ldg(w_seq + g) * (double)pow2f(-c) * (kEpsAcc * 448.0 * l1 + kConvAbs * 448.0);
+    term = __fmul_ru(__fmul_ru(__ldg(w_seq + g), pow2f(-c)), __fadd_ru(__fmul_ru(kEpsAcc448, l1), kConvAbs448));
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) term += __shfl_xor_sync(0xffffffffu, term, o);
-  const double E = (double)smax * term * (1.0 + 1e-9) + (double)smax * 1e-30;
-  return E > 0.0 ? E : 0.0;   // also maps NaN to 0
+  for (int o = 16; o > 0; o >>= 1) term = __fadd_ru(term, __shfl_xor_sync(0xffffffffu, term, o));
+  const float E = __fadd_ru(__fmul_ru(__fmul_ru(smax, term), 1.0f + 0x1p-20f), smax * 1e-30f);
+  return E > 0.f ? E : 0.f;   // also maps NaN to 0
 }
 
-__device__ __forceinline__ float hi_cut(float theta, double E) {
-  return __double2float_ru((1.0 + 4.0 * kRel) * (double)theta + 2.0 * E * (1.0 + 4.0 * kRel));
+// Cuts of a threshold theta: every item above hi_cut is certainly above an item whose
+// approximate value is theta, every item below lo_cut certainly below (the bound is
+// |approx - exact| <= E + r * approx; the cuts take 4r for margin and round outward).
+__device__ __forceinline__ float hi_cut(float theta, float E) {
+  return __fadd_ru(__fmul_ru(1.0f + 4.0f * kRelF, theta), __fmul_ru(2.0f + 8.0f * kRelF, E));
 }
-__device__ __forceinline__ float lo_cut(float theta, double E) {
-  return __double2float_rd((1.0 - 4.0 * kRel) * (double)theta - 2.0 * E * (1.0 + 4.0 * kRel));
+__device__ __forceinline__ float lo_cut(float theta, float E) {
+  return __fsub_rd(__fmul_rd(1.0f - 4.0f * kRelF, theta), __fmul_ru(2.0f + 8.0f * kRelF, E));
 }
 
 // ------------------------------------------------------------------ approximate scores
@@ -674,7 +678,7 @@ __global__ void __launch_bounds__(256) collect_kernel(const __grid_constant__ Id
   constexpr int kPer = kCollectPer / 256;
   __shared__ int s_scan[8];
   __shared__ int s_misc[4];
-  __shared__ double s_E;
+  __shared__ float s_E;
   __shared__ uint32_t s_base;
   const int b = blockIdx.y;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -693,8 +697,8 @@ __global__ void __launch_bounds__(256) collect_kernel(const __grid_constant__ Id
   float thr = -FLT_MAX;
   if (nb > a.n_keep) {
     if (tid < 32) {
-      double E = seq_bound(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx,
-                           __uint_as_float(a.ws.smax[b]), tid);
+      const float E = seq_bound(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx,
+                                __uint_as_float(a.ws.smax[b]), tid);
       if (tid == 0) s_E = E;
     }
     const float th_low = hist_threshold_low(a.ws.hist + (int64_t)b * kHistBins, a.n_keep, s_scan, s_misc);
@@ -721,21 +725,246 @@ __global__ void __launch_bounds__(256) collect_kernel(const __grid_constant__ Id
   }
 }
 
-// ------------------------------------------------------------------ block finalisation and positions
+// ------------------------------------------------------------------ selection
 
-constexpr int kSelCta = 256;           // threads of the per-sequence selection kernels
-constexpr int kBitmapWords = 4096;     // one bit per block: 131,072 blocks (1M positions at block 8)
-constexpr int kCandSmem = 8192;        // candidates staged in shared memory (64 KB)
-constexpr int kPvalSmem = 16384;       // position scores staged in shared memory (64 KB)
-constexpr int kUncSmem = 1024;         // band entries kept in shared memory (more spill to global)
-constexpr int kFlagWords = kMaxSel * 16 / 32;   // one bit per candidate position (<= 65,536)
+// One CTA per sequence selects from items (block maxima or position scores):
+//   1. the histogram of the items' float bits (4096 bins, built by the kernel that scored
+//      them) gives the bin of the k-th largest approximate value;
+//   2. one pass over the staged items, a warp per 32-item word, marks the items that are
+//      certainly in (above the upper cut of the bin's upper edge) with ballots and counts
+//      the items near the bin (between the cuts of its edges); a second pass lists them;
+//   3. a radix selection over that list gives the exact k-th approximate value, whose cuts
+//      split the list into certainly in, certainly out and the band;
+//   4. band items are rescored exactly and ranked by (exact score desc, id asc).
+#ifndef CSA2_SEL_THREADS
+#define CSA2_SEL_THREADS 512
+#endif
+constexpr int kSelCta = CSA2_SEL_THREADS;
+constexpr int kSelWarps = kSelCta / 32;
+constexpr int kDirectBlocks = 16384;         // up to this many blocks a sequence's maxima are read directly
+constexpr int kStageItems = 16384;           // items staged in shared memory
+constexpr int kListCap = 2048;               // near-threshold items kept in shared memory
+constexpr int kIdWords = 4096;               // block-id bitmaps: 131,072 blocks
+constexpr int kItemWords = kMaxSel * 16 / 32;   // position-item bitmap: 65,536 items
+static_assert(kHistBins % kSelCta == 0, "histogram bins per thread");
+
+__device__ __forceinline__ float bin_lo(uint32_t bin) { return __uint_as_float(bin << kHistShift); }
+__device__ __forceinline__ float bin_hi(uint32_t bin) { return __uint_as_float((bin + 1u) << kHistShift); }
+
+// Top-down bins of the ka-th and kb-th largest (1-based; a k outside [1, total] is not
+// looked for) over kHistBins counts.  s_out = {bin_a, above_a, bin_b, above_b, total}.
+// Needs blockDim.x == kSelCta.
+template <class CountFn>
+__device__ void cta_find_bins(int ka, int kb, CountFn count, int *s_scan, int *s_out) {
+  constexpr int PER = kHistBins / kSelCta;
+  const int top = kHistBins - 1 - (int)threadIdx.x * PER;         // this thread's highest bin
+  int c[PER];
+  int sum = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) { c[i] = (int)count(top - i); sum += c[i]; }
+  const int excl = cta_excl_scan(sum, s_scan);
+  if (threadIdx.x == 0) s_out[4] = s_scan[64];
+  if (excl < ka && ka <= excl + sum) {
+    int run = excl;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (run + c[i] >= ka) { s_out[0] = top - i; s_out[1] = run; break; }
+      run += c[i];
+    }
+  }
+  if (excl < kb && kb <= excl + sum) {
+    int run = excl;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if (run + c[i] >= kb) { s_out[2] = top - i; s_out[3] = run; break; }
+      run += c[i];
+    }
+  }
+  __syncthreads();
+}
+
+// r-th largest key (1 <= r <= matching items) among list entries, whose keys minus `base`
+// lie in [0, range]: radix passes of up to 11 bits over the list only.
+template <class KeyFn>
+__device__ uint32_t list_kth(const int32_t *m, int cnt, KeyFn key, int r, uint32_t base, uint32_t range,
+                             uint32_t *s_hist, int *s_scan, int *s_out) {
+  const int tid = threadIdx.x;
+  int shift = range ? 32 - __clz((int)range) : 0;
+  uint32_t prefix = 0;
+  while (shift > 0) {
+    const int w = min(11, shift);
+    const int sub = shift - w;
+    const int nbins = 1 << w;
+    for (int i = tid; i < nbins; i += blockDim.x) s_hist[i] = 0u;
+    __syncthreads();
+    for (int j = tid; j < cnt; j += blockDim.x) {
+      const uint32_t d = key(m[j]) - base;
+      const bool match = shift >= 32 || (d >> shift) == prefix;
+      if (match) atomicAdd(&s_hist[(d >> sub) & (uint32_t)(nbins - 1)], 1u);
+    }
+    __syncthreads();
+    cta_find_bin(nbins, r, [&](int bb) { return s_hist[bb]; }, s_scan, s_out);
+    prefix = (prefix << w) | (uint32_t)s_out[0];
+    r -= s_out[1];
+    shift = sub;
+  }
+  return base + prefix;
+}
+
+// Marks the top `need` band entries by (exact score desc, id asc); a warp per entry.
+template <class IdFn, class PickFn>
+__device__ void rank_band(const int32_t *band, const float2 *ex, int u, int need, IdFn id, PickFn pick) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  for (int i = warp; i < u; i += nwarps) {
+    const float2 vi = ex[i];
+    const int32_t ii = id(band[i]);
+    int rank = 0;
+    for (int m = lane; m < u; m += 32) {
+      const float2 vm = ex[m];
+      rank += df_greater(vm, vi) || (df_equal(vm, vi) && id(band[m]) < ii);
+    }
+    rank = __reduce_add_sync(0xffffffffu, rank);
+    if (lane == 0 && rank < need) pick(band[i]);
+  }
+}
+
+// Exact maxima of band blocks, one warp per block.  The block's rows are first scored on
+// the tensor cores; only rows whose upper bound reaches the best lower bound of the block
+// are rescored exactly (usually one).
+template <int BLOCK, class IdFn>
+__device__ void exact_block_maxima(const IdxArgs &a, const SeqTable &e, const QFrag &f, const QExact &q, float E,
+                                   const int32_t *band, float2 *ex, int u, IdFn id, const int32_t *lut) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int g = lane >> 2, t = lane & 3;
+  const float up = 1.0f + 2.0f * kRelF, dn = 1.0f - 2.0f * kRelF;
+  for (int i = warp; i < u; i += nwarps) {
+    const int32_t j = id(band[i]);
+    const int rg = g, rg8 = g + 8;
+    const int64_t p0 = (int64_t)j * BLOCK + rg, p8 = (int64_t)j * BLOCK + rg8;
+    const bool v0 = rg < BLOCK && p0 < e.len, v8 = rg8 < BLOCK && p8 < e.len;
+    const uint4 k0 = v0 ? ld_nc16(a.c.ik_codes + (e.base + p0) * kDIdx + 16 * t) : make_uint4(0, 0, 0, 0);
+    const uint4 k8 = v8 ? ld_nc16(a.c.ik_codes + (e.base + p8) * kDIdx + 16 * t) : make_uint4(0, 0, 0, 0);
+    const float s0 = v0 ? __ldg(a.c.ik_scale + e.base + p0) : 0.f;
+    const float s8 = v8 ? __ldg(a.c.ik_scale + e.base + p8) : 0.f;
+    float o0, o8;
+    score16(f, k0, k8, s0, s8, o0, o8);
+    const float lo0 = v0 ? __fsub_rd(__fmul_rd(dn, o0), E) : -FLT_MAX;
+    const float lo8 = v8 ? __fsub_rd(__fmul_rd(dn, o8), E) : -FLT_MAX;
+    const float best_lo = fmaxf(0.f, warp_max(fmaxf(lo0, lo8)));
+    const float hi0 = __fadd_ru(__fmul_ru(up, o0), E), hi8 = __fadd_ru(__fmul_ru(up, o8), E);
+    // rows that can still be the block's maximum
+    unsigned cand = __ballot_sync(0xffffffffu, t == 0 && v0 && hi0 >= best_lo);
+    unsigned cand8 = __ballot_sync(0xffffffffu, t == 0 && v8 && hi8 >= best_lo);
+    float2 best = make_float2(-1.f, 0.f);
+    while (cand | cand8) {
+      const bool from8 = cand == 0u;
+      const int src = __ffs(from8 ? cand8 : cand) - 1;          // lane t = 0 of the row's quad
+      if (from8) cand8 &= cand8 - 1; else cand &= cand - 1;
+      const uint4 kk = make_uint4(__shfl_sync(0xffffffffu, from8 ? k8.x : k0.x, src + t),
+                                  __shfl_sync(0xffffffffu, from8 ? k8.y : k0.y, src + t),
+                                  __shfl_sync(0xffffffffu, from8 ? k8.z : k0.z, src + t),
+                                  __shfl_sync(0xffffffffu, from8 ? k8.w : k0.w, src + t));
+      const float ss = __shfl_sync(0xffffffffu, from8 ? s8 : s0, src);
+      const float2 v = exact_sigma(q, kk, ss, lut);
+      if (df_greater(v, best)) best = v;
+    }
+    if (lane == 0) ex[i] = best;
+  }
+}
+
+enum { kCntIn = 0, kCntBand = 1, kCntPcb = 2, kCntSort = 3 };
+
+// Steps 3-4 for one threshold: exact k-th approximate value among the listed items, then
+// marks (via pick) the listed items that belong to the top k.  Every thread calls it.
+// `m`/`mc`: the near list; n_cert items above it are already marked.
+template <class ValFn, class IdFn, class ExactFn, class PickFn>
+__device__ void resolve_list(const int32_t *m, int mc, int k, int n_cert, float w_lo, float w_hi, float E, ValFn val,
+                             IdFn id, ExactFn exact_band, PickFn pick, int32_t *band, float2 *ex, uint32_t *s_hist,
+                             int *s_cnt, int *s_scan, int *s_out) {
+  const int r = k - n_cert;
+  const uint32_t kth = list_kth(m, mc, [&](int i) { return __float_as_uint(val(i)); }, r, __float_as_uint(w_lo),
+                                __float_as_uint(w_hi) - __float_as_uint(w_lo), s_hist, s_scan, s_out);
+  const float theta = __uint_as_float(kth);
+  const float hi = hi_cut(theta, E), lo = lo_cut(theta, E);
+  if (threadIdx.x == 0) { s_cnt[kCntIn] = 0; s_cnt[kCntBand] = 0; }
+  __syncthreads();
+  const int iters = (mc + blockDim.x - 1) / blockDim.x;
+  for (int it = 0; it < iters; ++it) {
+    const int j = it * blockDim.x + threadIdx.x;
+    const int i = j < mc ? m[j] : 0;
+    const float v = j < mc ? val(i) : -1.f;
+    const bool in = j < mc && v > hi;
+    const bool bd = j < mc && !in && v >= lo;
+    if (warp_reserve(in, &s_cnt[kCntIn]) >= 0) pick(i);
+    const int s = warp_reserve(bd, &s_cnt[kCntBand]);
+    if (bd) band[s] = i;
+  }
+  __syncthreads();
+  const int n_in = s_cnt[kCntIn], u = s_cnt[kCntBand];
+  if (u > 0) exact_band(band, ex, u);
+  __syncthreads();
+  rank_band(band, ex, u, r - n_in, id, pick);
+}
+
+// Warp-per-word classification of items [0, n) against up to two thresholds (a, b): each
+// 32-item word's "certain" ballot goes to cert_word(w, bits) (or to pick one by one), the
+// "near" items are counted per warp and then listed in item order.  Returns nothing; the
+// lists and counts are left in m_a / m_b and s_tot = {near_a, near_b, cert_a, cert_b}.
+struct NearLists {
+  int32_t *sa, *sb;      // shared lists (kListCap)
+  int32_t *ga, *gb;      // global lists (used when a list exceeds kListCap)
+};
+template <class ValFn, class CertFn>
+__device__ void classify_words(int n, ValFn val, bool use_a, float a_lo, float a_hi, bool use_b, float b_lo,
+                               float b_hi, CertFn cert, const NearLists &L, int (*s_wc)[4], int *s_tot) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int nw = (n + 31) / 32;
+  int na = 0, nbb = 0, ca = 0, cb = 0;
+  for (int w = warp; w < nw; w += nwarps) {
+    const int i = 32 * w + lane;
+    const float v = i < n ? val(i) : -1.f;
+    const bool ok = v >= 0.f;
+    const unsigned c1 = __ballot_sync(0xffffffffu, use_a && ok && v > a_hi);
+    const unsigned n1 = __ballot_sync(0xffffffffu, use_a && ok && v <= a_hi && v >= a_lo);
+    const unsigned c2 = __ballot_sync(0xffffffffu, use_b && ok && v > b_hi);
+    const unsigned n2 = __ballot_sync(0xffffffffu, use_b && ok && v <= b_hi && v >= b_lo);
+    cert(w, i, c1, c2);
+    na += __popc(n1); nbb += __popc(n2); ca += __popc(c1); cb += __popc(c2);
+  }
+  if (lane == 0) { s_wc[warp][0] = na; s_wc[warp][1] = nbb; s_wc[warp][2] = ca; s_wc[warp][3] = cb; }
+  __syncthreads();
+  int oa = 0, ob = 0, ta = 0, tb = 0, tca = 0, tcb = 0;
+  for (int x = 0; x < nwarps; ++x) {
+    if (x < warp) { oa += s_wc[x][0]; ob += s_wc[x][1]; }
+    ta += s_wc[x][0]; tb += s_wc[x][1]; tca += s_wc[x][2]; tcb += s_wc[x][3];
+  }
+  if (threadIdx.x == 0) { s_tot[0] = ta; s_tot[1] = tb; s_tot[2] = tca; s_tot[3] = tcb; }
+  int32_t *la = ta <= kListCap ? L.sa : L.ga;
+  int32_t *lb = tb <= kListCap ? L.sb : L.gb;
+  const unsigned lt = (1u << lane) - 1u;
+  for (int w = warp; w < nw; w += nwarps) {
+    const int i = 32 * w + lane;
+    const float v = i < n ? val(i) : -1.f;
+    const bool ok = v >= 0.f;
+    const bool in_a = use_a && ok && v <= a_hi && v >= a_lo;
+    const bool in_b = use_b && ok && v <= b_hi && v >= b_lo;
+    const unsigned n1 = __ballot_sync(0xffffffffu, in_a);
+    const unsigned n2 = __ballot_sync(0xffffffffu, in_b);
+    if (in_a) la[oa + __popc(n1 & lt)] = i;
+    if (in_b) lb[ob + __popc(n2 & lt)] = i;
+    oa += __popc(n1);
+    ob += __popc(n2);
+  }
+  __syncthreads();
+}
 
 // Approximate scores of the positions of an ascending block list (units of 16 positions;
 // this warp takes units u_first, u_first + u_step, ...; the loads of four units are issued
-// before any arithmetic).  Invalid positions score -1.
+// before any arithmetic).  Invalid positions score -1; valid ones are also counted in the
+// sequence's score histogram.
 template <int BLOCK>
 __device__ void score_units(const IdxArgs &a, const SeqTable &e, int64_t nb, const int32_t *list, int n, float *pv,
-                            const QFrag &f, int u_first, int u_step, float &smx) {
+                            uint32_t *hist, const QFrag &f, int u_first, int u_step, float &smx) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int units = (n + 15) / 16;
   for (int u0 = u_first; u0 < units; u0 += 4 * u_step) {
@@ -768,326 +997,206 @@ __device__ void score_units(const IdxArgs &a, const SeqTable &e, int64_t nb, con
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       if (u0 + j * u_step >= units) break;
-      float o0, o1;
-      score16(f, k[j][0], k[j][1], s[j][0], s[j][1], o0, o1);
+      float o[2];
+      score16(f, k[j][0], k[j][1], s[j][0], s[j][1], o[0], o[1]);
       smx = fmaxf(smx, fmaxf(s[j][0], s[j][1]));
       if (t == 0) {
-        const int i0 = (u0 + j * u_step) * 16 + g;
-        if (i0 < n) pv[i0] = ok[j][0] ? o0 : -1.f;
-        if (i0 + 8 < n) pv[i0 + 8] = ok[j][1] ? o1 : -1.f;
-      }
-    }
-  }
-}
-
-// Ranks `u` band entries (ids ascending <=> ties to the lower id) by exact score and calls
-// pick(id) for those of rank < need.
-template <class PickFn>
-__device__ void rank_band(const int32_t *ids, const float2 *vals, int u, int need, PickFn pick) {
-  for (int i = threadIdx.x; i < u; i += blockDim.x) {
-    const float2 vi = vals[i];
-    const int32_t ii = ids[i];
-    int rank = 0;
-    for (int m = 0; m < u; ++m) {
-      const float2 vm = vals[m];
-      rank += df_greater(vm, vi) || (df_equal(vm, vi) && ids[m] < ii);
-    }
-    if (rank < need) pick(ii);
-  }
-}
-
-// Exact maxima of `u` band blocks, one warp per block.  The block's rows are first scored
-// on the tensor cores; only rows whose upper bound reaches the best lower bound of the
-// block are rescored exactly (usually one).
-template <int BLOCK>
-__device__ void exact_block_maxima(const IdxArgs &a, const SeqTable &e, const QFrag &f, const QExact &q, double E,
-                                   const int32_t *unc_id, float2 *unc_val, int u, const int32_t *lut) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int g = lane >> 2, t = lane & 3;
-  for (int i = warp; i < u; i += nwarps) {
-    const int32_t j = unc_id[i];
-    float best_lo = 0.f;
-    float2 best = make_float2(-1.f, 0.f);
-    for (int r0 = 0; r0 < BLOCK; r0 += 16) {                 // 16 rows per pass (one for BLOCK <= 8)
-      const int rg = r0 + g, rg8 = r0 + g + 8;
-      const int64_t p0 = (int64_t)j * BLOCK + rg, p8 = (int64_t)j * BLOCK + rg8;
-      const bool v0 = rg < BLOCK && p0 < e.len, v8 = rg8 < BLOCK && p8 < e.len;
-      const uint4 k0 = v0 ? ld_nc16(a.c.ik_codes + (e.base + p0) * kDIdx + 16 * t) : make_uint4(0, 0, 0, 0);
-      const uint4 k8 = v8 ? ld_nc16(a.c.ik_codes + (e.base + p8) * kDIdx + 16 * t) : make_uint4(0, 0, 0, 0);
-      const float s0 = v0 ? __ldg(a.c.ik_scale + e.base + p0) : 0.f;
-      const float s8 = v8 ? __ldg(a.c.ik_scale + e.base + p8) : 0.f;
-      float o0, o8;
-      score16(f, k0, k8, s0, s8, o0, o8);
-      // bounds of each row's exact score
-      const float lo0 = v0 ? __double2float_rd((1.0 - 2.0 * kRel) * o0 - E) : -FLT_MAX;
-      const float lo8 = v8 ? __double2float_rd((1.0 - 2.0 * kRel) * o8 - E) : -FLT_MAX;
-      best_lo = fmaxf(best_lo, warp_max(fmaxf(lo0, lo8)));
-      const float hi0 = v0 ? __double2float_ru((1.0 + 2.0 * kRel) * o0 + E) : -FLT_MAX;
-      const float hi8 = v8 ? __double2float_ru((1.0 + 2.0 * kRel) * o8 + E) : -FLT_MAX;
-      // rows that can still be the block's maximum
-      unsigned cand = __ballot_sync(0xffffffffu, t == 0 && v0 && hi0 >= best_lo) & 0x11111111u;
-      unsigned cand8 = __ballot_sync(0xffffffffu, t == 0 && v8 && hi8 >= best_lo) & 0x11111111u;
-      while (cand | cand8) {
-        const bool from8 = cand == 0u;
-        const int src = __ffs(from8 ? cand8 : cand) - 1;      // lane of the quad holding the row
-        if (from8) cand8 &= cand8 - 1; else cand &= cand - 1;
-        const uint4 kk = make_uint4(__shfl_sync(0xffffffffu, from8 ? k8.x : k0.x, src + t),
-                                    __shfl_sync(0xffffffffu, from8 ? k8.y : k0.y, src + t),
-                                    __shfl_sync(0xffffffffu, from8 ? k8.z : k0.z, src + t),
-                                    __shfl_sync(0xffffffffu, from8 ? k8.w : k0.w, src + t));
-        const float ss = __shfl_sync(0xffffffffu, from8 ? s8 : s0, src);
-        const float2 v = exact_sigma(q, kk, ss, lut);
-        if (df_greater(v, best)) best = v;
-      }
-    }
-    if (lane == 0) unc_val[i] = best;
-  }
-}
-
-// Exact top-k positions among n candidates with approximate scores pv[i] (-1 invalid);
-// candidate i is position list[i/BLOCK]*BLOCK + i%BLOCK, ascending in i.  Writes the
-// selected positions ascending to out[0..topk), -1 padded.  Every thread calls it.
-struct SelSmem {
-  uint32_t *hist;      // [4096]
-  uint32_t *flag;      // [n/32]
-  int32_t *unc_id;     // [kUncSmem]
-  float2 *unc_val;     // [kUncSmem]
-  int *cnt;            // [8]
-  int *scan;           // [72]
-  int *out;            // [4]
-  const int32_t *lut;  // [256]
-};
-
-template <int BLOCK>
-__device__ void select_topk(const IdxArgs &a, const SeqTable &e, int b, const int32_t *list, int n, const float *pv,
-                            double E, int32_t *out, const SelSmem &sm) {
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
-  const int nwords = (n + 31) / 32;
-  auto pos_of = [&](int i) -> int32_t { return list[i / BLOCK] * BLOCK + (i % BLOCK); };
-  for (int i = tid; i < nwords; i += blockDim.x) sm.flag[i] = 0u;
-  for (int i = tid; i < kHistBins; i += blockDim.x) sm.hist[i] = 0u;
-  if (tid < 8) sm.cnt[tid] = 0;
-  __syncthreads();
-  const int iters = (n + blockDim.x - 1) / blockDim.x;
-  int nvalid = 0;
-  for (int it = 0; it < iters; ++it) {                       // histogram of the valid scores
-    const int i = it * blockDim.x + tid;
-    const float v = i < n ? pv[i] : -1.f;
-    const bool valid = v >= 0.f;
-    const unsigned act = __ballot_sync(0xffffffffu, valid);
-    nvalid += __popc(act);
-    if (valid) {
-      const uint32_t bin = min(score_key(v) >> kHistShift, (uint32_t)kHistBins - 1);
-      const unsigned grp = __match_any_sync(act, bin);
-      if (lane == __ffs(grp) - 1) atomicAdd(&sm.hist[bin], (uint32_t)__popc(grp));
-    }
-  }
-  if (lane == 0) atomicAdd(&sm.cnt[3], nvalid);
-  __syncthreads();
-  const int n_valid = sm.cnt[3];
-  const int k = min(a.topk, n_valid);
-  if (n_valid <= a.topk) {
-    for (int i = tid; i < n; i += blockDim.x)
-      if (pv[i] >= 0.f) atomicOr(&sm.flag[i >> 5], 1u << (i & 31));
-  } else {
-    cta_find_bin(kHistBins, k, [&](int bin) { return sm.hist[bin]; }, sm.scan, sm.out);
-    const uint32_t bin = (uint32_t)sm.out[0];
-    const int above = sm.out[1];
-    const uint32_t kth =
-        cta_kth_in_bin(n, k - above, [&](int i) { return pv[i] >= 0.f ? score_key(pv[i]) : 0u; }, bin, sm.hist,
-                       sm.scan, sm.out);
-    const float theta = __uint_as_float(kth);
-    const float hi = hi_cut(theta, E), lo = lo_cut(theta, E);
-    int32_t *g_id = a.ws.unc_id + (int64_t)b * a.ws.unc_cap;
-    float2 *g_val = a.ws.unc_val + (int64_t)b * a.ws.unc_cap;
-    for (int it = 0; it < iters; ++it) {
-      const int i = it * blockDim.x + tid;
-      const float v = i < n ? pv[i] : -1.f;
-      const bool in = v >= 0.f && v > hi;
-      const bool unc = v >= 0.f && !in && v >= lo;
-      if (warp_reserve(in, &sm.cnt[0]) >= 0) atomicOr(&sm.flag[i >> 5], 1u << (i & 31));
-      const int su = warp_reserve(unc, &sm.cnt[1]);
-      if (unc) {
-        if (su < kUncSmem) sm.unc_id[su] = i; else g_id[su] = i;   // candidate index, ascending = position order
-      }
-    }
-    __syncthreads();
-    const int n_in = sm.cnt[0], u = sm.cnt[1];
-    const bool small = u <= kUncSmem;
-    int32_t *ids = small ? sm.unc_id : g_id;
-    float2 *vals = small ? sm.unc_val : g_val;
-    if (!small)
-      for (int i = tid; i < kUncSmem; i += blockDim.x) g_id[i] = sm.unc_id[i];
-    __syncthreads();
-    if (u > 0) {
-      QExact q;
-      load_qexact(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx, lane, q);
-      for (int i = warp; i < u; i += nwarps) {
-        const int64_t row = e.base + pos_of(ids[i]);
-        const uint4 kk = __ldg(reinterpret_cast<const uint4 *>(a.c.ik_codes + row * kDIdx + 16 * (lane & 3)));
-        const float2 v = exact_sigma(q, kk, __ldg(a.c.ik_scale + row), sm.lut);
-        if (lane == 0) vals[i] = v;
-      }
-    }
-    __syncthreads();
-    rank_band(ids, vals, u, k - n_in, [&](int32_t ii) { atomicOr(&sm.flag[ii >> 5], 1u << (ii & 31)); });
-  }
-  __syncthreads();
-  emit_bits_ascending(sm.flag, nwords, pos_of, out, a.topk, sm.scan);
-}
-
-// The Full layer after the scan: the pool (top n_keep blocks, exact) and the ascending list
-// of blocks that may hold a top-k position (every block whose upper bound reaches the
-// lower bound of the k-th largest block maximum).
-template <int BLOCK>
-__global__ void __launch_bounds__(kSelCta) finalize_blocks_kernel(const __grid_constant__ IdxArgs a) {
-  extern __shared__ __align__(16) uint64_t s_cand[];
-  __shared__ uint32_t s_hist[1024];
-  __shared__ uint32_t s_bits[kBitmapWords];
-  __shared__ int32_t s_unc_id[kUncSmem];
-  __shared__ float2 s_unc_val[kUncSmem];
-  __shared__ int32_t s_lut[256];
-  __shared__ int s_cnt[8];
-  __shared__ int s_scan[72];
-  __shared__ int s_out[4];
-  __shared__ double s_E;
-  const int b = blockIdx.x;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
-  const int64_t nb = (e.len + BLOCK - 1) / BLOCK;
-  const int n_keep = a.n_keep;
-  const int k1 = (int)min((int64_t)n_keep, nb);
-  const int c = (int)a.ws.cand_cnt[b];
-  const uint64_t *cand_g = a.ws.cand + (int64_t)b * a.ws.nbm;
-  const uint32_t *hist_g = a.ws.hist + (int64_t)b * kHistBins;
-  int32_t *pool = a.pool_out + (int64_t)b * n_keep;
-  int32_t *pcb = a.ws.pcb + (int64_t)b * n_keep;
-  const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
-  const float *wb = a.w + (int64_t)b * kHIdx;
-  const bool use_bits = nb <= (int64_t)kBitmapWords * 32;
-  const int nwords = (int)((nb + 31) / 32);
-  const bool staged = c <= kCandSmem;
-  if (staged)
-    for (int i = tid; i < c; i += blockDim.x) s_cand[i] = __ldcg(cand_g + i);
-  const uint64_t *cand = staged ? s_cand : cand_g;
-  fill_e4m3_lut(s_lut);
-  if (warp == 0) {
-    double E = seq_bound(qb, wb, __uint_as_float(a.ws.smax[b]), lane);
-    if (lane == 0) s_E = E;
-  }
-  if (tid < 8) s_cnt[tid] = 0;
-  if (use_bits)
-    for (int i = tid; i < nwords; i += blockDim.x) s_bits[i] = 0u;
-  __syncthreads();
-  const double E = s_E;
-  const int iters = (c + blockDim.x - 1) / blockDim.x;
-  auto cval = [&](int i) { return __uint_as_float((uint32_t)(cand[i] >> 32)); };
-  auto ckey = [&](int i) { return (uint32_t)(cand[i] >> 32); };
-  auto cid = [&](int i) { return (int32_t)(uint32_t)cand[i]; };
-  int32_t *list_fallback = a.ws.unc_id + (int64_t)b * a.ws.unc_cap;   // only without the bitmap
-  auto mark = [&](int32_t j, int slot) {
-    if (use_bits) atomicOr(&s_bits[j >> 5], 1u << (j & 31));
-    else if (slot >= 0) list_fallback[slot] = j;
-  };
-  // the k-th largest approximate block maximum: its histogram bin, then two radix passes
-  auto kth_block = [&](int k) {
-    cta_find_bin(kHistBins, k, [&](int bin) { return __ldcg(hist_g + bin); }, s_scan, s_out);
-    const uint32_t bin = (uint32_t)s_out[0];
-    const int above = s_out[1];
-    return __uint_as_float(cta_kth_in_bin(c, k - above, ckey, bin, s_hist, s_scan, s_out));
-  };
-
-  // ---- pool: the top k1 blocks by (exact block score desc, id asc)
-  if (nb <= n_keep) {
-    for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < nb ? i : -1;
-  } else {
-    const float theta = kth_block(k1);
-    const float hi = hi_cut(theta, E), lo = lo_cut(theta, E);
-    int32_t *g_id = a.ws.unc_id + (int64_t)b * a.ws.unc_cap + a.ws.nbm;       // past the fallback list
-    float2 *g_val = a.ws.unc_val + (int64_t)b * a.ws.unc_cap;
-    for (int it = 0; it < iters; ++it) {
-      const int i = it * blockDim.x + tid;
-      const float v = i < c ? cval(i) : -1.f;
-      const bool in = i < c && v > hi;
-      const bool unc = i < c && !in && v >= lo;
-      const int s_in = warp_reserve(in, &s_cnt[0]);
-      if (in) mark(cid(i), s_in);
-      const int s_un = warp_reserve(unc, &s_cnt[1]);
-      if (unc) {
-        if (s_un < kUncSmem) s_unc_id[s_un] = cid(i); else g_id[s_un] = cid(i);
-      }
-    }
-    __syncthreads();
-    const int n_in = s_cnt[0], u = s_cnt[1];
-    const bool small = u <= kUncSmem;
-    int32_t *ids = small ? s_unc_id : g_id;
-    float2 *vals = small ? s_unc_val : g_val;
-    if (!small)
-      for (int i = tid; i < kUncSmem; i += blockDim.x) g_id[i] = s_unc_id[i];
-    __syncthreads();
-    if (u > 0) {
-      QFrag f;
-      QExact q;
-      load_qfrag(qb, wb, lane, f);
-      load_qexact(qb, wb, lane, q);
-      exact_block_maxima<BLOCK>(a, e, f, q, E, ids, vals, u, s_lut);
-    }
-    __syncthreads();
-    rank_band(ids, vals, u, k1 - n_in, [&](int32_t ji) {
-      if (use_bits) atomicOr(&s_bits[ji >> 5], 1u << (ji & 31));
-      else list_fallback[atomicAdd(&s_cnt[0], 1)] = ji;
-    });
-    __syncthreads();
-    if (use_bits) {
-      emit_bits_ascending(s_bits, nwords, [](int i) { return (int32_t)i; }, pool, n_keep, s_scan);
-    } else {
-      // without the bitmap (more than 131,072 blocks): order the k1 ids through the global list
-      __syncthreads();
-      for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < k1 ? list_fallback[i] : -1;
-      __syncthreads();
-      if (tid == 0) {   // insertion sort of at most n_keep ids; this path serves contexts > 1M at block 8
-        for (int i = 1; i < k1; ++i) {
-          const int32_t v = pool[i];
-          int j = i - 1;
-          while (j >= 0 && pool[j] > v) { pool[j + 1] = pool[j]; --j; }
-          pool[j + 1] = v;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int i = (u0 + j * u_step) * 16 + g + 8 * h;
+          if (i < n) {
+            pv[i] = ok[j][h] ? o[h] : -1.f;
+            if (ok[j][h]) atomicAdd(&hist[min(__float_as_uint(o[h]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+          }
         }
       }
     }
   }
+}
+
+// ---- the Full layer after the scan: pool + position-candidate blocks
+
+// Pool = the top min(n_keep, nb) blocks by (exact block score desc, id asc), ascending.
+// Position-candidate blocks = every block whose approximate maximum reaches the lower cut
+// of the topk-th largest approximate block maximum (they contain every top-k position),
+// ascending.  DIRECT: the sequence's block maxima are the items (nb <= kDirectBlocks);
+// otherwise the items are the candidates gathered by collect_kernel.  Both thresholds
+// come from the scan's histogram of all block maxima.
+template <int BLOCK, bool DIRECT>
+__global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __grid_constant__ IdxArgs a) {
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn);            // radix scratch [2048]
+  uint32_t *s_pool_bits = s_hist + 2048;
+  uint32_t *s_pcb_bits = s_pool_bits + kIdWords;
+  int32_t *s_m1 = reinterpret_cast<int32_t *>(s_pcb_bits + kIdWords);
+  int32_t *s_m2 = s_m1 + kListCap;
+  int32_t *s_band = s_m2 + kListCap;
+  float2 *s_ex = reinterpret_cast<float2 *>(s_band + kListCap);
+  int32_t *s_lut = reinterpret_cast<int32_t *>(s_ex + kListCap);
+  float *s_val = reinterpret_cast<float *>(s_lut + 256);
+  int32_t *s_id = reinterpret_cast<int32_t *>(s_val + kStageItems);  // candidate mode only
+  __shared__ int s_cnt[8];
+  __shared__ int s_scan[72];
+  __shared__ int s_out[8];
+  __shared__ int s_wc[kSelWarps][4];
+  __shared__ int s_tot[4];
+  __shared__ float s_E;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
+  const int nb = (int)((e.len + BLOCK - 1) / BLOCK);
+  const int n_keep = a.n_keep;
+  const int k1 = min(n_keep, nb), k2 = min(a.topk, nb);
+  const bool sel_pool = nb > n_keep, sel_pcb = nb > a.topk;
+  int32_t *pool = a.pool_out + (int64_t)b * n_keep;
+  int32_t *pcb = a.ws.pcb + (int64_t)b * n_keep;
+  const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
+  const float *wb = a.w + (int64_t)b * kHIdx;
+  const uint32_t *hist_g = a.ws.hist + (int64_t)b * kHistBins;
+  const uint64_t *cand_g = a.ws.cand + (int64_t)b * a.ws.nbm;
+  const bool use_bits = nb <= kIdWords * 32;
+  const int nwords = use_bits ? (nb + 31) / 32 : 0;
+
+  if (!DIRECT)
+    for (int i = tid; i < nwords; i += blockDim.x) { s_pool_bits[i] = 0u; s_pcb_bits[i] = 0u; }
+  if (tid < 8) s_cnt[tid] = 0;
+  fill_e4m3_lut(s_lut);
+  if (warp == 0) {
+    const float E = seq_bound(qb, wb, __uint_as_float(a.ws.smax[b]), lane);
+    if (lane == 0) s_E = E;
+  }
+  // ---- stage the items
+  int n;
+  bool staged = true;
+  if (DIRECT) {
+    n = nb;
+    const float *bm = a.ws.bmax + (int64_t)b * a.ws.nbm;            // 16-byte aligned rows
+    const int n4 = n >> 2;
+    for (int i = tid; i < n4; i += blockDim.x)
+      reinterpret_cast<float4 *>(s_val)[i] = __ldcg(reinterpret_cast<const float4 *>(bm) + i);
+    for (int i = 4 * n4 + tid; i < n; i += blockDim.x) s_val[i] = __ldcg(bm + i);
+  } else {
+    n = (int)a.ws.cand_cnt[b];
+    staged = n <= kStageItems;
+    if (staged) {
+      const int n2 = n >> 1;
+      for (int i = tid; i < n2; i += blockDim.x) {
+        const uint4 v = __ldcg(reinterpret_cast<const uint4 *>(cand_g) + i);
+        s_val[2 * i] = __uint_as_float(v.y); s_id[2 * i] = (int32_t)v.x;
+        s_val[2 * i + 1] = __uint_as_float(v.w); s_id[2 * i + 1] = (int32_t)v.z;
+      }
+      if ((n & 1) && tid == 0) {
+        const uint64_t v = __ldcg(cand_g + n - 1);
+        s_val[n - 1] = __uint_as_float((uint32_t)(v >> 32)); s_id[n - 1] = (int32_t)(uint32_t)v;
+      }
+    }
+  }
+  // ---- histogram bins of the k1-th and k2-th largest block maxima (syncs the staging)
+  cta_find_bins(sel_pool ? k1 : 0, sel_pcb ? k2 : 0, [&](int bin) { return __ldcg(hist_g + bin); }, s_scan, s_out);
+  const uint32_t bin1 = sel_pool ? (uint32_t)s_out[0] : 0u, bin2 = sel_pcb ? (uint32_t)s_out[2] : 0u;
+  const float E = s_E;
+  const float w1_hi = hi_cut(bin_hi(bin1), E), w1_lo = lo_cut(bin_lo(bin1), E);
+  const float w2_hi = hi_cut(bin_hi(bin2), E), w2_lo = lo_cut(bin_lo(bin2), E);
+  auto val = [&](int i) -> float {
+    if (DIRECT || staged) return s_val[i];
+    return __uint_as_float((uint32_t)(__ldcg(cand_g + i) >> 32));
+  };
+  auto id = [&](int i) -> int32_t {
+    if (DIRECT) return i;
+    if (staged) return s_id[i];
+    return (int32_t)(uint32_t)__ldcg(cand_g + i);
+  };
+  // the sort buffer of the no-bitmap path reuses the pcb bitmap (pcb = pool there)
+  int32_t *s_sort = reinterpret_cast<int32_t *>(s_pcb_bits);
+  auto pick_pool = [&](int i) {
+    const int32_t j = id(i);
+    if (use_bits) atomicOr(&s_pool_bits[j >> 5], 1u << (j & 31));
+    else s_sort[atomicAdd(&s_cnt[kCntSort], 1)] = j;
+  };
+  auto pick_pcb = [&](int i) {
+    const int32_t j = id(i);
+    if (use_bits) atomicOr(&s_pcb_bits[j >> 5], 1u << (j & 31));
+  };
+  auto cert = [&](int w, int i, unsigned c1, unsigned c2) {
+    if (DIRECT) {                                                   // item words are id words
+      if (lane == 0) { s_pool_bits[w] = c1; s_pcb_bits[w] = c2; }
+    } else {
+      if ((c1 >> lane) & 1u) pick_pool(i);
+      if ((c2 >> lane) & 1u) pick_pcb(i);
+    }
+  };
+  int32_t *g_m1 = a.ws.unc_id + (int64_t)b * 3 * a.ws.unc_x;       // lists beyond kListCap
+  int32_t *g_m2 = g_m1 + a.ws.unc_x;
+  classify_words(n, val, sel_pool, w1_lo, w1_hi, sel_pcb, w2_lo, w2_hi, cert, NearLists{s_m1, s_m2, g_m1, g_m2},
+                 s_wc, s_tot);
+  const int m1c = s_tot[0], m2c = s_tot[1], cert1 = s_tot[2], cert2 = s_tot[3];
+  const int32_t *m1 = m1c <= kListCap ? s_m1 : g_m1;
+  const int32_t *m2 = m2c <= kListCap ? s_m2 : g_m2;
+
+  // ---- pool
+  if (sel_pool) {
+    const bool big = m1c > kListCap;
+    int32_t *band = big ? g_m1 + 2 * a.ws.unc_x : s_band;
+    float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : s_ex;
+    auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
+      QFrag f;
+      QExact q;
+      load_qfrag(qb, wb, lane, f);
+      load_qexact(qb, wb, lane, q);
+      exact_block_maxima<BLOCK>(a, e, f, q, E, bd, xv, u, id, s_lut);
+    };
+    resolve_list(m1, m1c, k1, cert1, w1_lo, w1_hi, E, val, id, exact_band, pick_pool, band, ex, s_hist, s_cnt,
+                 s_scan, s_out);
+  }
+  __syncthreads();
+  // ---- position-candidate blocks: the topk-th largest approximate maximum, lower cut
+  if (sel_pcb) {
+    const uint32_t kth = list_kth(m2, m2c, [&](int i) { return __float_as_uint(val(i)); }, k2 - cert2,
+                                  __float_as_uint(w2_lo), __float_as_uint(w2_hi) - __float_as_uint(w2_lo), s_hist,
+                                  s_scan, s_out);
+    const float lo2 = lo_cut(__uint_as_float(kth), E);
+    for (int j = tid; j < m2c; j += blockDim.x) {
+      const int i = m2[j];
+      if (val(i) >= lo2) pick_pcb(i);
+    }
+  }
   __syncthreads();
 
-  // ---- position-candidate blocks (ascending)
-  if (nb <= a.topk) {
-    for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = i < nb ? i : -1;
-    if (tid == 0) a.ws.pcb_cnt[b] = (uint32_t)nb;
-    return;
-  }
-  const float lo2 = lo_cut(kth_block(a.topk), E);
-  if (use_bits)
-    for (int i = tid; i < nwords; i += blockDim.x) s_bits[i] = 0u;
-  if (tid == 0) s_cnt[2] = 0;
-  __syncthreads();
-  for (int it = 0; it < iters; ++it) {
-    const int i = it * blockDim.x + tid;
-    const bool keep = i < c && cval(i) >= lo2;
-    const int slot = warp_reserve(keep, &s_cnt[2]);
-    if (keep) mark(cid(i), slot);
-  }
-  __syncthreads();
-  const int n_pcb = s_cnt[2];
-  if (n_pcb > n_keep || !use_bits) {
-    // a pathological band (or no bitmap): the pool always contains them, already ascending
-    for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = pool[i];
-    if (tid == 0) a.ws.pcb_cnt[b] = (uint32_t)k1;
+  // ---- emit, ascending
+  if (!sel_pool) {
+    for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < nb ? i : -1;
+  } else if (use_bits) {
+    emit_bits_ascending(s_pool_bits, nwords, [](int i) { return (int32_t)i; }, pool, n_keep, s_scan);
   } else {
-    emit_bits_ascending(s_bits, nwords, [](int i) { return (int32_t)i; }, pcb, n_keep, s_scan);
-    if (tid == 0) a.ws.pcb_cnt[b] = (uint32_t)n_pcb;
+    cta_sort_asc(s_sort, k1);                                     // k1 <= n_keep <= 4096 ids
+    for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < k1 ? s_sort[i] : -1;
   }
+  __syncthreads();
+  int n_pcb;
+  if (!sel_pcb) {
+    for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = i < nb ? i : -1;
+    n_pcb = nb;
+  } else {
+    int cnt = 0;
+    if (use_bits)
+      for (int i = tid; i < nwords; i += blockDim.x) cnt += __popc(s_pcb_bits[i]);
+    cnt = __reduce_add_sync(0xffffffffu, cnt);
+    if (lane == 0) atomicAdd(&s_cnt[kCntPcb], cnt);
+    __syncthreads();
+    n_pcb = s_cnt[kCntPcb];
+    if (!use_bits || n_pcb > n_keep) {
+      // the pool contains every top-k position's block and is already ascending
+      for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = pool[i];
+      n_pcb = k1;
+    } else {
+      emit_bits_ascending(s_pcb_bits, nwords, [](int i) { return (int32_t)i; }, pcb, n_keep, s_scan);
+    }
+  }
+  if (tid == 0) a.ws.pcb_cnt[b] = (uint32_t)n_pcb;
 }
 
 // Scores of the positions of a block list (the Full layer's candidate blocks, or the pool
-// for a Reindex layer), many CTAs per sequence.
+// for a Reindex layer), many CTAs per sequence, with their histogram.
 template <int BLOCK>
 __global__ void __launch_bounds__(256) score_positions_kernel(const __grid_constant__ IdxArgs a) {
   const int b = blockIdx.y;
@@ -1099,93 +1208,145 @@ __global__ void __launch_bounds__(256) score_positions_kernel(const __grid_const
   if (a.use_pool) { list = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
   else { list = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
   const int n = count * BLOCK;
-  float *pv = a.ws.pvals + (int64_t)b * a.n_keep * BLOCK;
+  float *pv = a.ws.pvals + (int64_t)b * a.ws.pv_stride;
   QFrag f;
   load_qfrag(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx, lane, f);
   float smx = 0.f;
-  score_units<BLOCK>(a, e, nb, list, n, pv, f, blockIdx.x * 8 + warp, gridDim.x * 8, smx);
+  score_units<BLOCK>(a, e, nb, list, n, pv, a.ws.hist2 + (int64_t)b * kHistBins, f, blockIdx.x * 8 + warp,
+                     gridDim.x * 8, smx);
   smx = warp_max(smx);
   if (lane == 0 && smx > 0.f) atomicMax(&a.ws.smax2[b], __float_as_uint(smx));
 }
 
-// Exact top-k over the scored positions (the Full layer's candidates, or a Reindex pool).
-template <int BLOCK>
-__global__ void __launch_bounds__(kSelCta) select_positions_kernel(const __grid_constant__ IdxArgs a) {
-  extern __shared__ __align__(16) float s_pv[];
-  __shared__ uint32_t s_hist[kHistBins];
-  __shared__ uint32_t s_flag[kFlagWords];
-  __shared__ int32_t s_unc_id[kUncSmem];
-  __shared__ float2 s_unc_val[kUncSmem];
-  __shared__ int32_t s_lut[256];
+// Exact top-k over the scored positions (the Full layer's candidates, or a Reindex pool),
+// written ascending.  STAGED: the scores fit in shared memory (n_keep * BLOCK <= kStageItems).
+template <int BLOCK, bool STAGED>
+__global__ void __launch_bounds__(kSelCta, 1) select_positions_kernel(const __grid_constant__ IdxArgs a) {
+  extern __shared__ __align__(16) uint8_t s_dyn[];
+  uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn);            // radix scratch [2048]
+  uint32_t *s_bits = s_hist + 2048;
+  int32_t *s_m = reinterpret_cast<int32_t *>(s_bits + kItemWords);
+  int32_t *s_band = s_m + kListCap;
+  float2 *s_ex = reinterpret_cast<float2 *>(s_band + kListCap);
+  int32_t *s_lut = reinterpret_cast<int32_t *>(s_ex + kListCap);
+  int32_t *s_list = s_lut + 256;                                     // [kMaxSel]
+  float *s_pv = reinterpret_cast<float *>(s_list + kMaxSel);         // [kStageItems] when STAGED
   __shared__ int s_cnt[8];
   __shared__ int s_scan[72];
-  __shared__ int s_out[4];
-  __shared__ double s_E;
+  __shared__ int s_out[8];
+  __shared__ int s_wc[kSelWarps][4];
+  __shared__ int s_tot[4];
+  __shared__ float s_E;
   const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
-  const int32_t *list;
+  const int32_t *list_g;
   int count;
-  if (a.use_pool) { list = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
-  else { list = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
+  if (a.use_pool) { list_g = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
+  else { list_g = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
   const int n = count * BLOCK;
-  const float *pv_g = a.ws.pvals + (int64_t)b * a.n_keep * BLOCK;
-  const bool staged = n <= kPvalSmem;
-  if (staged)
-    for (int i = tid; i < n; i += blockDim.x) s_pv[i] = __ldcg(pv_g + i);
-  if (a.use_pool)
-    for (int i = tid + 1; i < count; i += blockDim.x) {
-      const int32_t v = __ldg(list + i);
-      if (v >= 0 && __ldg(list + i - 1) >= v) set_err(a.d_err, CSA2_DEVERR_POOL);   // the pool must ascend
-    }
+  const int nwords = (n + 31) / 32;
+  const float *pv_g = a.ws.pvals + (int64_t)b * a.ws.pv_stride;     // 16-byte aligned rows
+  const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
+  const float *wb = a.w + (int64_t)b * kHIdx;
+  const uint32_t *hist_g = a.ws.hist2 + (int64_t)b * kHistBins;
+
+  if (tid < 8) s_cnt[tid] = 0;
+  for (int i = tid; i < count; i += blockDim.x) s_list[i] = __ldg(list_g + i);
   fill_e4m3_lut(s_lut);
   if (warp == 0) {
-    double E = seq_bound(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx, __uint_as_float(a.ws.smax2[b]),
-                         lane);
+    const float E = seq_bound(qb, wb, __uint_as_float(a.ws.smax2[b]), lane);
     if (lane == 0) s_E = E;
   }
+  if (STAGED) {
+    const int n4 = n >> 2;
+    for (int i = tid; i < n4; i += blockDim.x)
+      reinterpret_cast<float4 *>(s_pv)[i] = __ldcg(reinterpret_cast<const float4 *>(pv_g) + i);
+    for (int i = 4 * n4 + tid; i < n; i += blockDim.x) s_pv[i] = __ldcg(pv_g + i);
+  }
+  // the bin of the topk-th largest score, and the number of valid scores (syncs the staging)
+  cta_find_bins(a.topk, 0, [&](int bin) { return __ldcg(hist_g + bin); }, s_scan, s_out);
+  const int n_valid = s_out[4];
+  const float E = s_E;
+  if (a.use_pool)                                                   // the pool must ascend
+    for (int i = tid + 1; i < count; i += blockDim.x)
+      if (s_list[i] >= 0 && s_list[i - 1] >= s_list[i]) set_err(a.d_err, CSA2_DEVERR_POOL);
+  auto val = [&](int i) -> float { return STAGED ? s_pv[i] : __ldcg(pv_g + i); };
+  auto id = [](int i) -> int32_t { return i; };                      // item order = position order
+  auto pick = [&](int i) { atomicOr(&s_bits[i >> 5], 1u << (i & 31)); };
+  auto pos_of = [&](int i) -> int32_t { return s_list[i / BLOCK] * BLOCK + (i % BLOCK); };
+  auto cert = [&](int w, int, unsigned c1, unsigned) { if (lane == 0) s_bits[w] = c1; };
+  int32_t *g_m = a.ws.unc_id + (int64_t)b * 3 * a.ws.unc_x;
+  if (n_valid <= a.topk) {
+    // every valid score is selected: "certain" = valid, nothing near
+    classify_words(n, val, true, 1.f, -0.5f, false, 0.f, 0.f, cert, NearLists{s_m, s_m, g_m, g_m}, s_wc, s_tot);
+  } else {
+    const uint32_t bin = (uint32_t)s_out[0];
+    const float w_hi = hi_cut(bin_hi(bin), E), w_lo = lo_cut(bin_lo(bin), E);
+    classify_words(n, val, true, w_lo, w_hi, false, 0.f, 0.f, cert, NearLists{s_m, s_m, g_m, g_m}, s_wc, s_tot);
+    const int mc = s_tot[0], n_cert = s_tot[2];
+    const bool big = mc > kListCap;
+    const int32_t *m = big ? g_m : s_m;
+    int32_t *band = big ? g_m + a.ws.unc_x : s_band;
+    float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : s_ex;
+    auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
+      QExact q;
+      load_qexact(qb, wb, lane, q);
+      for (int j = warp; j < u; j += kSelWarps) {
+        const int64_t row = e.base + pos_of(bd[j]);
+        const uint4 kk = __ldg(reinterpret_cast<const uint4 *>(a.c.ik_codes + row * kDIdx + 16 * (lane & 3)));
+        const float2 v = exact_sigma(q, kk, __ldg(a.c.ik_scale + row), s_lut);
+        if (lane == 0) xv[j] = v;
+      }
+    };
+    resolve_list(m, mc, a.topk, n_cert, w_lo, w_hi, E, val, id, exact_band, pick, band, ex, s_hist, s_cnt, s_scan,
+                 s_out);
+  }
   __syncthreads();
-  SelSmem sm{s_hist, s_flag, s_unc_id, s_unc_val, s_cnt, s_scan, s_out, s_lut};
-  select_topk<BLOCK>(a, e, b, list, n, staged ? s_pv : pv_g, s_E, a.topk_out + (int64_t)b * a.topk, sm);
+  emit_bits_ascending(s_bits, nwords, pos_of, a.topk_out + (int64_t)b * a.topk, a.topk, s_scan);
 }
 
 // ------------------------------------------------------------------ test: bounds
 
 __global__ void bound_kernel(const __grid_constant__ IdxArgs a, double *bound) {
   const int b = blockIdx.x;
-  double E = seq_bound(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx,
-                       __uint_as_float(a.ws.smax[b]), threadIdx.x);
-  if (threadIdx.x == 0) bound[b] = E;
-  if (b == 0 && threadIdx.x == 0) bound[a.c.B] = kRel;
+  const float E = seq_bound(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx,
+                            __uint_as_float(a.ws.smax[b]), threadIdx.x);
+  if (threadIdx.x == 0) bound[b] = (double)E;
+  if (b == 0 && threadIdx.x == 0) bound[a.c.B] = (double)kRelF;
 }
 
 // ------------------------------------------------------------------ host side
 
 static size_t align_up(size_t x) { return (x + 255) & ~(size_t)255; }
 
+static int64_t round4(int64_t x) { return (x + 3) & ~(int64_t)3; }
+
 size_t indexer_ws_bytes(int32_t B, int64_t max_len, int32_t block, int32_t n_keep) {
-  const int64_t nbm = (max_len + block - 1) / block;
-  const int64_t npos = (int64_t)n_keep * block;
-  const int64_t unc = nbm + (nbm > npos ? nbm : npos);
-  size_t z = align_up((size_t)B * kHistBins * 4) + 4 * align_up((size_t)B * 4);
+  const int64_t nbm = round4((max_len + block - 1) / block);
+  const int64_t npos = round4((int64_t)n_keep * block);
+  const int64_t unc = nbm > npos ? nbm : npos;
+  size_t z = 2 * align_up((size_t)B * kHistBins * 4) + 4 * align_up((size_t)B * 4);
   size_t s = z;
   s += align_up((size_t)B * nbm * 4);       // bmax
   s += align_up((size_t)B * nbm * 8);       // cand
   s += align_up((size_t)B * n_keep * 4);    // pcb
   s += align_up((size_t)B * npos * 4);      // pvals
-  s += align_up((size_t)B * unc * 4);       // unc_id
+  s += align_up((size_t)B * unc * 12);      // unc_id: three lists per sequence
   s += align_up((size_t)B * unc * 8);       // unc_val
   return s;
 }
 
 IndexerWs indexer_ws_carve(void *ws, int32_t B, int64_t max_len, int32_t block, int32_t n_keep) {
   IndexerWs w;
-  const int64_t nbm = (max_len + block - 1) / block;
-  const int64_t npos = (int64_t)n_keep * block;
+  const int64_t nbm = round4((max_len + block - 1) / block);
+  const int64_t npos = round4((int64_t)n_keep * block);
   w.nbm = nbm;
-  w.unc_cap = nbm + (nbm > npos ? nbm : npos);
+  w.pv_stride = npos;
+  w.unc_x = nbm > npos ? nbm : npos;
   char *p = (char *)ws;
   w.hist = (uint32_t *)p; p += align_up((size_t)B * kHistBins * 4);
+  w.hist2 = (uint32_t *)p; p += align_up((size_t)B * kHistBins * 4);
   w.smax = (uint32_t *)p; p += align_up((size_t)B * 4);
   w.smax2 = (uint32_t *)p; p += align_up((size_t)B * 4);
   w.cand_cnt = (uint32_t *)p; p += align_up((size_t)B * 4);
@@ -1195,7 +1356,7 @@ IndexerWs indexer_ws_carve(void *ws, int32_t B, int64_t max_len, int32_t block, 
   w.cand = (uint64_t *)p; p += align_up((size_t)B * nbm * 8);
   w.pcb = (int32_t *)p; p += align_up((size_t)B * n_keep * 4);
   w.pvals = (float *)p; p += align_up((size_t)B * npos * 4);
-  w.unc_id = (int32_t *)p; p += align_up((size_t)B * w.unc_cap * 4);
+  w.unc_id = (int32_t *)p; p += align_up((size_t)B * w.unc_x * 12);
   w.unc_val = (float2 *)p;
   return w;
 }
@@ -1231,17 +1392,41 @@ static int scan_grid_size(int B, int64_t max_len) {
   return (int)std::max<int64_t>(g, 1);
 }
 
+constexpr size_t kFinalizeSmemDirect =
+    (size_t)(2048 + 2 * kIdWords) * 4 + (size_t)3 * kListCap * 4 + (size_t)kListCap * 8 + 256 * 4 +
+    (size_t)kStageItems * 4;
+constexpr size_t kFinalizeSmemCand = kFinalizeSmemDirect + (size_t)kStageItems * 4;
+constexpr size_t kSelectSmemBase = (size_t)(2048 + kItemWords) * 4 + (size_t)2 * kListCap * 4 +
+                                   (size_t)kListCap * 8 + 256 * 4 + (size_t)kMaxSel * 4;
+constexpr size_t kSelectSmemStaged = kSelectSmemBase + (size_t)kStageItems * 4;
+
 template <int BLOCK>
 static void select_smem_optin() {
   static bool done = false;
   if (!done) {
-    cudaFuncSetAttribute(finalize_blocks_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCandSmem * 8);
-    cudaFuncSetAttribute(select_positions_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kPvalSmem * 4);
+    cudaFuncSetAttribute(finalize_blocks_kernel<BLOCK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kFinalizeSmemDirect);
+    cudaFuncSetAttribute(finalize_blocks_kernel<BLOCK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kFinalizeSmemCand);
+    cudaFuncSetAttribute(select_positions_kernel<BLOCK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSelectSmemStaged);
+    cudaFuncSetAttribute(select_positions_kernel<BLOCK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)kSelectSmemBase);
     done = true;
   }
 }
 
 static int positions_grid(int B) { return std::max(1, std::min(32, (int)((int64_t)num_sms() * 2 / std::max(B, 1)))); }
+
+template <int BLOCK>
+static void launch_positions(IdxArgs &a, cudaStream_t st) {
+  const int B = a.c.B;
+  score_positions_kernel<BLOCK><<<dim3(positions_grid(B), B), 256, 0, st>>>(a);
+  if ((int64_t)a.n_keep * BLOCK <= kStageItems)
+    select_positions_kernel<BLOCK, true><<<B, kSelCta, kSelectSmemStaged, st>>>(a);
+  else
+    select_positions_kernel<BLOCK, false><<<B, kSelCta, kSelectSmemBase, st>>>(a);
+}
 
 template <int BLOCK>
 static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_profile *prof, cudaStream_t st) {
@@ -1256,20 +1441,21 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
   scan_kernel<BLOCK><<<scan_grid, kScanWarps * 32, scan_smem_bytes(B), st>>>(a);
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
   const int64_t nbm = a.ws.nbm;
-  dim3 cg((unsigned)((nbm + kCollectPer - 1) / kCollectPer), (unsigned)B);
-  collect_kernel<BLOCK><<<cg, 256, 0, st>>>(a);
-  finalize_blocks_kernel<BLOCK><<<B, kSelCta, kCandSmem * 8, st>>>(a);
-  score_positions_kernel<BLOCK><<<dim3(positions_grid(B), B), 256, 0, st>>>(a);
-  select_positions_kernel<BLOCK><<<B, kSelCta, kPvalSmem * 4, st>>>(a);
+  if (nbm <= kDirectBlocks) {
+    finalize_blocks_kernel<BLOCK, true><<<B, kSelCta, kFinalizeSmemDirect, st>>>(a);
+  } else {
+    dim3 cg((unsigned)((nbm + kCollectPer - 1) / kCollectPer), (unsigned)B);
+    collect_kernel<BLOCK><<<cg, 256, 0, st>>>(a);
+    finalize_blocks_kernel<BLOCK, false><<<B, kSelCta, kFinalizeSmemCand, st>>>(a);
+  }
+  launch_positions<BLOCK>(a, st);
   return cudaGetLastError();
 }
 
 template <int BLOCK>
 static cudaError_t reindex_impl(IdxArgs &a, cudaStream_t st) {
-  const int B = a.c.B;
   select_smem_optin<BLOCK>();
-  score_positions_kernel<BLOCK><<<dim3(positions_grid(B), B), 256, 0, st>>>(a);
-  select_positions_kernel<BLOCK><<<B, kSelCta, kPvalSmem * 4, st>>>(a);
+  launch_positions<BLOCK>(a, st);
   return cudaGetLastError();
 }
 

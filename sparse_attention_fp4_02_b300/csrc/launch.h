@@ -19,7 +19,8 @@ cudaError_t launch_test_fp8(const float *x, int64_t n, int C, uint8_t *codes, fl
 
 // ---- indexer ----
 struct IndexerWs {           // carved out of the caller's workspace
-  uint32_t *hist;            // [B][4096]
+  uint32_t *hist;            // [B][4096] scan: histogram of block maxima
+  uint32_t *hist2;           // [B][4096] position scores' histogram
   uint32_t *smax;            // [B]   scan's max key scale (float bits)
   uint32_t *smax2;           // [B]   position stage's max key scale
   uint32_t *cand_cnt;        // [B]
@@ -27,10 +28,11 @@ struct IndexerWs {           // carved out of the caller's workspace
   float *bmax;               // [B][nbm]
   uint64_t *cand;            // [B][nbm]
   int32_t *pcb;              // [B][n_keep]
-  float *pvals;              // [B][n_keep * block]
-  int32_t *unc_id;           // [B][unc_cap]
-  float2 *unc_val;           // [B][unc_cap] exact scores as normalised double-floats
-  int64_t nbm, unc_cap;
+  float *pvals;              // [B][pv_stride] position scores
+  int32_t *unc_id;           // [B][3][unc_x] item lists that overflow shared memory
+  float2 *unc_val;           // [B][unc_x] their exact scores as normalised double-floats
+  int64_t nbm, unc_x;        // block maxima per sequence (a multiple of 4), overflow list length
+  int64_t pv_stride;         // n_keep * block rounded up to a multiple of 4
   size_t zero_bytes;         // bytes at the start that must be zeroed per call
 };
 
