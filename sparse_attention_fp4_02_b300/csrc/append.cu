@@ -1,5 +1,7 @@
 // kv_append_fp4: RoPE + FP4 (E2M1 / E4M3 per 16 channels) main KV, FP8 indexer
-// key, FP8 SWA ring, one warp per token.
+// key, FP8 SWA ring.  One warp per (token, part): part 0 writes the main KV row and the
+// indexer key, part 1 + l the token's row of SWA layer l.  Every load a warp needs is
+// issued before it waits on any of them.
 // Method: origotech.dev deep dive, subsection "FP4와 SWA Bounded Replay" (FP4
 // main KV quantised after RoPE, SWA KV in FP8).
 #include "common.cuh"
@@ -62,17 +64,25 @@ __device__ __forceinline__ void load4_bf16(const uint16_t *p, float x[4]) {
 }
 
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendArgs a) {
+  pdl_enter();
   const int lane = threadIdx.x & 31;
-  const int64_t tok = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int parts = a.swa_new ? 1 + a.n_swa : 1;
+  const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t tok = wid / parts;
+  const int part = (int)(wid - tok * parts);
   if (tok >= a.n) return;
-  const int b = a.seq_id[tok];
-  const int64_t p = a.pos[tok];
+  // independent loads first: the token's identity and this part's input row
+  const int b = __ldg(a.seq_id + tok);
+  const int64_t p = __ldg(a.pos + tok);
+  const uint16_t *src = part == 0 ? a.kv_new + tok * kD : a.swa_new + ((int64_t)(part - 1) * a.n + tok) * kD;
+  const uint2 raw = __ldg(reinterpret_cast<const uint2 *>(src + 4 * lane));
+  uint32_t ik_raw = 0;
+  if (part == 0 && a.ik_new) ik_raw = __ldg(reinterpret_cast<const uint32_t *>(a.ik_new + tok * kDIdx + 2 * lane));
   if (b < 0 || b >= a.c.B) {
     if (lane == 0) set_err(a.d_err, CSA2_DEVERR_SEQ);
     return;
   }
-  const int64_t row = a.c.seq_base[b] + p;
-  if (p < 0 || p >= a.rope_len || row < 0 || row >= a.c.T_cap) {
+  if (p < 0 || p >= a.rope_len) {
     if (lane == 0) set_err(a.d_err, CSA2_DEVERR_POS);
     return;
   }
@@ -84,42 +94,41 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
     c0 = __ldg(cr + i0); s0 = __ldg(sr + i0);
     c1 = __ldg(cr + i0 + 1); s1 = __ldg(sr + i0 + 1);
   }
+  float x[4] = {bf16_to_f32(raw.x & 0xFFFFu), bf16_to_f32(raw.x >> 16), bf16_to_f32(raw.y & 0xFFFFu),
+                bf16_to_f32(raw.y >> 16)};
+  if (lane >= 16) { rotate(x[0], x[1], c0, s0); rotate(x[2], x[3], c1, s1); }
 
-  // main KV -> FP4
-  {
-    float x[4];
-    load4_bf16(a.kv_new + tok * kD + 4 * lane, x);
-    if (lane >= 16) { rotate(x[0], x[1], c0, s0); rotate(x[2], x[3], c1, s1); }
+  // a token whose cache row is out of range is skipped by every part
+  const int64_t row = a.c.seq_base[b] + p;
+  if (row < 0 || row >= a.c.T_cap) {
+    if (lane == 0) set_err(a.d_err, CSA2_DEVERR_POS);
+    return;
+  }
+  if (part == 0) {
+    // main KV -> FP4
     uint32_t scode;
     uint32_t packed = quant_fp4_lane(x, &scode);
     *reinterpret_cast<uint16_t *>(a.c.kv_codes + row * (kD / 2) + 2 * lane) = (uint16_t)packed;
     if ((lane & 3) == 0) a.c.kv_scales[row * (kD / 16) + (lane >> 2)] = (uint8_t)scode;
-  }
-  // indexer key -> FP8 with a per-token scale (no rotation)
-  if (a.ik_new) {
-    uint32_t raw = __ldg(reinterpret_cast<const uint32_t *>(a.ik_new + tok * kDIdx + 2 * lane));
-    float x0 = bf16_to_f32(raw & 0xFFFFu), x1 = bf16_to_f32(raw >> 16);
-    float am = warp_max(fmaxf(fabsf(x0), fabsf(x1)));
-    float s = __fdiv_rn(am, 448.0f);
-    uint32_t code = fp8_code(x0, s) | (fp8_code(x1, s) << 8);
-    *reinterpret_cast<uint16_t *>(a.c.ik_codes + row * kDIdx + 2 * lane) = (uint16_t)code;
-    if (lane == 0) a.c.ik_scale[row] = s;
-  }
-  // each SWA layer: rotate like the main KV, FP8 with a per-token scale, ring slot p % ring
-  if (a.swa_new) {
-    for (int l = 0; l < a.n_swa; ++l) {
-      float x[4];
-      load4_bf16(a.swa_new + ((int64_t)l * a.n + tok) * kD + 4 * lane, x);
-      if (lane >= 16) { rotate(x[0], x[1], c0, s0); rotate(x[2], x[3], c1, s1); }
-      float am = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    // indexer key -> FP8 with a per-token scale (no rotation)
+    if (a.ik_new) {
+      float x0 = bf16_to_f32(ik_raw & 0xFFFFu), x1 = bf16_to_f32(ik_raw >> 16);
+      float am = warp_max(fmaxf(fabsf(x0), fabsf(x1)));
       float s = __fdiv_rn(am, 448.0f);
-      uint32_t code = fp8_code(x[0], s) | (fp8_code(x[1], s) << 8) | (fp8_code(x[2], s) << 16) |
-                      (fp8_code(x[3], s) << 24);
-      const csa2_swa &w = a.swa[l];
-      const int64_t slot = (int64_t)b * w.ring + (p % w.ring);
-      *reinterpret_cast<uint32_t *>(w.codes + slot * kD + 4 * lane) = code;
-      if (lane == 0) w.scale[slot] = s;
+      uint32_t code = fp8_code(x0, s) | (fp8_code(x1, s) << 8);
+      *reinterpret_cast<uint16_t *>(a.c.ik_codes + row * kDIdx + 2 * lane) = (uint16_t)code;
+      if (lane == 0) a.c.ik_scale[row] = s;
     }
+  } else {
+    // SWA layer part - 1: rotated like the main KV, FP8 with a per-token scale, ring slot p % ring
+    float am = warp_max(fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3]))));
+    float s = __fdiv_rn(am, 448.0f);
+    uint32_t code = fp8_code(x[0], s) | (fp8_code(x[1], s) << 8) | (fp8_code(x[2], s) << 16) |
+                    (fp8_code(x[3], s) << 24);
+    const csa2_swa &w = a.swa[part - 1];
+    const int64_t slot = (int64_t)b * w.ring + (p % w.ring);
+    *reinterpret_cast<uint32_t *>(w.codes + slot * kD + 4 * lane) = code;
+    if (lane == 0) w.scale[slot] = s;
   }
 }
 
@@ -137,9 +146,9 @@ cudaError_t launch_append(const csa2_cache &c, const csa2_swa *swa, int n_swa, c
   a.cos = cos; a.sin = sin; a.rope_len = rope_len;
   a.seq_id = seq_id; a.pos = pos; a.n = n; a.d_err = d_err;
   const int warps = 8;
-  const int64_t grid = (n + warps - 1) / warps;
-  kv_append_kernel<<<(unsigned)grid, warps * 32, 0, st>>>(a);
-  return cudaGetLastError();
+  const int64_t parts = swa_new ? 1 + n_swa : 1;
+  const int64_t grid = (n * parts + warps - 1) / warps;
+  return launch_k(kv_append_kernel, dim3((unsigned)grid), dim3(warps * 32), 0, st, 0, a);
 }
 
 // ---- test-only kernels: the same quantisers on raw float32 data ----

@@ -5,15 +5,17 @@
 // "CSA2와 어텐션 재설계" (128-token local window combined with global sparse retrieval);
 // origotech.dev deep dive, subsection "Compressed Sparse Attention 2(CSA2)" (top-k 512).
 //
-// One CTA per (query row, group of 16 heads), kAttnWarps warps.  The CTA first loads the
-// row's top-k indices into shared memory and its queries (bf16 -> f16) next to them; each
-// warp then owns a contiguous run of 16-row tiles and streams their raw rows (packed FP4
-// codes + E4M3 group scales, or FP8 window rows + their float32 scale) through a
-// kAttnRing-slot cp.async ring, so every gather of the warp is in flight before the first
-// tile is computed.  A tile is dequantised exactly to f16 in shared memory and consumed by
-// mma.sync: S = Q K^T (M = 16 heads), online softmax in f32, O += P V with P split into f16
-// hi + lo parts (P V error ~2^-22).  Warps merge (m, l, O) through padded shared-memory
-// slices.  No CTA waits on another CTA and nothing is allocated.
+// A cluster of `split` CTAs per (query row, group of 16 heads) shares the row's tiles:
+// each warp of each CTA owns a contiguous run of 16-row tiles and streams their raw rows
+// (packed FP4 codes + E4M3 group scales, or FP8 window rows + their float32 scale) through
+// a kAttnRing-slot cp.async ring, so every gather of the warp is in flight before the
+// first tile is computed.  A tile is dequantised exactly to f16 in shared memory and
+// consumed by mma.sync: S = Q K^T (M = 16 heads), online softmax in f32, O += P V with P
+// split into f16 hi + lo parts (P V error ~2^-22).  Warps merge (m, l, O) through padded
+// shared-memory slices; the CTAs of a cluster then send their partial (m, l, O) into the
+// first CTA's shared memory (distributed shared memory), which merges and writes the row.
+// Short batches of rows use larger clusters so that the whole GPU takes part.  Nothing is
+// allocated and no CTA waits on a CTA outside its cluster.
 //
 // Exactness of the operands: an E2M1 value times its E4M3 group scale has at most 6
 // significant bits within [2^-10, 2688] and is exact in f16; an E4M3 value is exact in
@@ -34,7 +36,8 @@ constexpr int kStride = 136;          // halfs per f16 tile row: 128 + 8 (confli
 constexpr int kSlot = 2112;           // raw tile: FP4 16 x (64 + 8) = 1,152 B; FP8 16 x 128 + 16 x 4 = 2,112 B
 constexpr int kAttnRing = 4;          // raw tile slots per warp
 constexpr int kOStride = 132;         // floats per merge-slice row
-constexpr int kMaxTopk = 4096;
+constexpr int kMaxSplit = 8;           // CTAs per cluster (portable maximum)
+constexpr int kPartFloats = 16 * kD + 32;                           // one CTA's partial: O, m, l
 constexpr int kTileBytes = kTileRows * kStride * 2;                 // 4,352 B
 constexpr int kRingBytes = kAttnRing * kSlot;                       // 8,448 B (= 16 x 132 x 4)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -53,7 +56,7 @@ struct AttnArgs {
   float tau;
   float *out, *lse;
   int tiles_sel, tiles_win;
-  int idx_bytes;          // shared bytes reserved for the indices (16-byte multiple)
+  int split;              // CTAs per cluster sharing one row's tiles
   int32_t *d_err;
 };
 
@@ -71,6 +74,35 @@ __device__ __forceinline__ void sts128(uint16_t *dst, uint32_t a, uint32_t b, ui
   *reinterpret_cast<uint4 *>(dst) = make_uint4(a, b, c, d);
 }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+// shared address of the same variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t smem_addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(smem_addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};\n" ::"r"(addr), "f"(v.x), "f"(v.y), "f"(v.z),
+               "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;\n" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __grid_constant__ AttnArgs a) {
   extern __shared__ __align__(16) uint8_t s_dyn[];
   __shared__ __align__(16) uint16_t s_q[16 * kStride];
@@ -79,12 +111,17 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
   __shared__ float s_m[kAttnWarps][16], s_l[kAttnWarps][16];
   __shared__ float s_cm[16], s_cl[16];
 
-  const int t = blockIdx.x, hg = blockIdx.y;
+  pdl_enter();
+  const int split = a.split;
+  const int t = blockIdx.x / split, hg = blockIdx.y;
+  const int crank = split > 1 ? (int)cluster_rank() : 0;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
-  int32_t *s_idx = reinterpret_cast<int32_t *>(s_dyn);
-  uint16_t *tile = reinterpret_cast<uint16_t *>(s_dyn + a.idx_bytes + warp * kTileBytes);
-  uint8_t *ring = s_dyn + a.idx_bytes + kAttnWarps * kTileBytes + warp * kRingBytes;
+  uint16_t *tile = reinterpret_cast<uint16_t *>(s_dyn + warp * kTileBytes);
+  uint8_t *ring = s_dyn + kAttnWarps * kTileBytes + warp * kRingBytes;
+  float *s_part = reinterpret_cast<float *>(s_dyn + kAttnWarps * (kTileBytes + kRingBytes));   // [split][kPartFloats]
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
+  // every CTA of the cluster has started before any writes into another's shared memory
+  if (split > 1) cluster_arrive_relaxed();
 
   // ---- the query row and its sequence
   const int b = a.q_seq[t];
@@ -96,33 +133,29 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     len = a.c.seq_len[b];
     ok = p >= 0 && p < len && base >= 0 && base + len <= a.c.T_cap;
   }
-  if (!ok && hg == 0 && tid == 0) set_err(a.d_err, (b < 0 || b >= a.c.B) ? CSA2_DEVERR_SEQ : CSA2_DEVERR_POS);
+  if (!ok && hg == 0 && crank == 0 && tid == 0)
+    set_err(a.d_err, (b < 0 || b >= a.c.B) ? CSA2_DEVERR_SEQ : CSA2_DEVERR_POS);
 
-  // ---- indices and queries, loaded together
-  for (int i = tid; i < a.topk; i += blockDim.x) s_idx[i] = __ldg(a.topk_idx + (int64_t)t * a.topk + i);
-  for (int i = tid; i < 16 * 16; i += blockDim.x) {        // 16 heads x 16 chunks of 8 values
-    const int h = i >> 4, c8 = i & 15;
-    const uint4 v = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8));
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) o[j] = pack_f16x2(bf16_to_f32(w[j] & 0xFFFFu), bf16_to_f32(w[j] >> 16));
-    sts128(s_q + h * kStride + 8 * c8, o[0], o[1], o[2], o[3]);
+  // ---- queries (bf16 -> f16 into shared memory); their loads overlap the first gathers
+  uint4 qv = make_uint4(0, 0, 0, 0);
+  if (tid < 256) {                                            // 16 heads x 16 chunks of 8 values
+    const int h = tid >> 4, c8 = tid & 15;
+    qv = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8));
   }
-  __syncthreads();
 
-  // ---- this warp's tiles and their gathers
+  // ---- this warp's tiles: the row's tiles are split evenly over every warp of the cluster
   const int n_tiles = ok ? a.tiles_sel + a.tiles_win : 0;
-  const int per_w = (n_tiles + kAttnWarps - 1) / kAttnWarps;
-  const int tw0 = min(n_tiles, warp * per_w), tw1 = min(n_tiles, tw0 + per_w);
+  const int slots = split * kAttnWarps, slot_id = crank * kAttnWarps + warp;
+  const int tw0 = (int)((int64_t)n_tiles * slot_id / slots), tw1 = (int)((int64_t)n_tiles * (slot_id + 1) / slots);
   const int swa_ring = a.swa.ring;
   const int r = lane >> 1, hf = lane & 1;
+  const int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
   auto issue = [&](int ti, int slot) {
     const uint32_t dst = ring_s + slot * kSlot;
     bool valid = false;
     if (ti < a.tiles_sel) {
       const int j = ti * kTileRows + r;
-      const int32_t idx = j < a.topk ? s_idx[j] : -1;
+      const int32_t idx = j < a.topk ? __ldg(idx_row + j) : -1;
       if (idx >= 0) {
         if (idx > p) { if (hf == 0) set_err(a.d_err, CSA2_DEVERR_INDEX); }
         else valid = true;
@@ -151,6 +184,15 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     if (tw0 + s < tw1) issue(tw0 + s, s);
     else cp_async_commit();
   }
+  if (tid < 256) {
+    const int h = tid >> 4, c8 = tid & 15;
+    const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+    uint32_t o4[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o4[j] = pack_f16x2(bf16_to_f32(w[j] & 0xFFFFu), bf16_to_f32(w[j] >> 16));
+    sts128(s_q + h * kStride + 8 * c8, o4[0], o4[1], o4[2], o4[3]);
+  }
+  __syncthreads();
 
   // Q fragments (A operand of S = Q K^T) through ldmatrix: heads g (a0, a2) and g + 8 (a1, a3)
   uint32_t qa[8][4];
@@ -323,14 +365,64 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
   }
   __syncthreads();
   const int64_t head0 = (int64_t)t * a.H + 16 * hg;
-  const uint8_t *rings = s_dyn + a.idx_bytes + kAttnWarps * kTileBytes;
-  for (int i = tid; i < 16 * 32; i += blockDim.x) {         // 4 consecutive dims per thread
+  const uint8_t *rings = s_dyn + kAttnWarps * kTileBytes;
+  if (split == 1) {
+    for (int i = tid; i < 16 * 32; i += blockDim.x) {       // 4 consecutive dims per thread
+      const int h = i >> 5, d4 = (i & 31) * 4;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int w = 0; w < kAttnWarps; ++w) {
+        const float4 v = *reinterpret_cast<const float4 *>(rings + w * kRingBytes + (h * kOStride + d4) * 4);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      }
+      const float l = s_cl[h];
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      *reinterpret_cast<float4 *>(a.out + (head0 + h) * kD + d4) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    }
+    if (a.lse && tid < 16) a.lse[head0 + tid] = s_cl[tid] > 0.f ? s_cm[tid] + logf(s_cl[tid]) : -INFINITY;
+    return;
+  }
+  // ---- cluster merge: every CTA sends (O, m, l) into slot crank of the first CTA
+  cluster_wait_acquire();                                      // every CTA of the cluster is running
+  const uint32_t slot0 = map_to_rank((uint32_t)__cvta_generic_to_shared(s_part + crank * kPartFloats), 0);
+  for (int i = tid; i < 16 * 32; i += blockDim.x) {
     const int h = i >> 5, d4 = (i & 31) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int w = 0; w < kAttnWarps; ++w) {
       const float4 v = *reinterpret_cast<const float4 *>(rings + w * kRingBytes + (h * kOStride + d4) * 4);
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    st_cluster_v4(slot0 + (h * kD + d4) * 4, acc);
+  }
+  if (tid < 16) {
+    st_cluster_f32(slot0 + (16 * kD + tid) * 4, s_cm[tid]);
+    st_cluster_f32(slot0 + (16 * kD + 16 + tid) * 4, s_cl[tid]);
+  }
+  cluster_arrive_release();
+  cluster_wait_acquire();
+  if (crank != 0) return;
+  if (tid < 16) {
+    float M = -INFINITY, L = 0.f;
+    for (int q = 0; q < split; ++q) M = fmaxf(M, s_part[q * kPartFloats + 16 * kD + tid]);
+    for (int q = 0; q < split; ++q) {
+      const float mq = s_part[q * kPartFloats + 16 * kD + tid];
+      const float f = mq == -INFINITY ? 0.f : exp2f((mq - M) * kLog2e);
+      s_part[q * kPartFloats + 16 * kD + tid] = f;            // the partial's weight
+      L += s_part[q * kPartFloats + 16 * kD + 16 + tid] * f;
+    }
+    s_cm[tid] = M;
+    s_cl[tid] = L;
+  }
+  __syncthreads();
+  for (int i = tid; i < 16 * 32; i += blockDim.x) {
+    const int h = i >> 5, d4 = (i & 31) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < split; ++q) {
+      const float f = s_part[q * kPartFloats + 16 * kD + h];
+      const float4 v = *reinterpret_cast<const float4 *>(s_part + q * kPartFloats + h * kD + d4);
+      acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
     }
     const float l = s_cl[h];
     const float inv = l > 0.f ? 1.f / l : 0.f;
@@ -342,12 +434,19 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
 
 // ------------------------------------------------------------------ host side
 
-static int attn_idx_bytes(int topk) { return ((topk * 4 + 15) / 16) * 16; }
-static size_t attn_smem(int topk) {
-  return (size_t)attn_idx_bytes(topk) + (size_t)kAttnWarps * (kTileBytes + kRingBytes);
+static size_t attn_smem(int split) {
+  return (size_t)kAttnWarps * (kTileBytes + kRingBytes) + (split > 1 ? (size_t)split * kPartFloats * 4 : 0);
 }
 
 size_t attn_ws_bytes(int64_t, int32_t, int32_t, int32_t) { return 0; }
+
+// CTAs per cluster: the largest power of two (<= 8) that keeps every (row, head group)
+// cluster resident at once, one CTA per SM.
+static int attn_split(int64_t rows) {
+  int split = 1;
+  while (split < kMaxSplit && rows * split * 2 <= (int64_t)num_sms()) split *= 2;
+  return split;
+}
 
 cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const uint16_t *q, int H, int64_t T,
                                const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx, int topk,
@@ -356,7 +455,7 @@ cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const u
   if (T == 0) return cudaSuccess;
   static bool optin = false;
   if (!optin) {
-    cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem(kMaxTopk));
+    cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem(kMaxSplit));
     optin = true;
   }
   AttnArgs a;
@@ -365,10 +464,9 @@ cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const u
   a.d_err = d_err;
   a.tiles_sel = (topk + kTileRows - 1) / kTileRows;
   a.tiles_win = (window + kTileRows - 1) / kTileRows;
-  a.idx_bytes = attn_idx_bytes(topk);
-  dim3 grid((unsigned)T, (unsigned)(H / 16));
-  attn_decode_kernel<<<grid, kAttnWarps * 32, attn_smem(topk), st>>>(a);
-  return cudaGetLastError();
+  a.split = attn_split(T * (H / 16));
+  return launch_k(attn_decode_kernel, dim3((unsigned)(T * a.split), (unsigned)(H / 16)), dim3(kAttnWarps * 32),
+                  attn_smem(a.split), st, (unsigned)a.split, a);
 }
 
 }  // namespace csa2

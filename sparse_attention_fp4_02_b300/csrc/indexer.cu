@@ -409,11 +409,6 @@ struct IdxArgs {
 
 // ------------------------------------------------------------------ scan
 
-// Each warp streams a contiguous range of 16-position units through its own cp.async
-// ring in shared memory (kScanStages stages of 32 rows), so loads in flight hold no
-// registers.  A warp's range is walked as per-sequence segments; a stage never mixes
-// sequences.  Stage layout: 32 rows x 64 key bytes, then 32 scales stored so that lane
-// quad g finds rows g, g+8, g+16, g+24 in one 16-byte word.
 #ifndef CSA2_SCAN_WARPS
 #define CSA2_SCAN_WARPS 8
 #endif
@@ -473,164 +468,190 @@ __device__ __forceinline__ float score32_row(const QFrag &f, const uint4 &ka, co
 }
 
 // Block maxima of one stage from per-lane row scores (lane (g, t) holds stage row 8t+g):
-// one redux over the lanes of each block, then the block's first lane writes it.
+// xor-shuffles over the lanes of each block (uniform across the warp), then the block's
+// first lane writes it and counts it in the histogram (the CTA's shared copy for its home
+// sequence, else the global one).  `rows`: valid rows of the stage; blk0: the stage's
+// first block id within the sequence.
 template <int BLOCK>
-__device__ __forceinline__ void emit_stage(float o, int lane, int64_t cp, int rows, int64_t L, float *bmax,
-                                           uint32_t *hist) {
+__device__ __forceinline__ void emit_stage(float o, int lane, int blk0, int rows, float *bmax, uint32_t *s_hist,
+                                           uint32_t *g_hist, bool home) {
   const int g = lane >> 2, t = lane & 3;
-  unsigned mask;
-  if constexpr (BLOCK == 16) mask = t < 2 ? 0x33333333u : 0xCCCCCCCCu;
-  else mask = (0x11111111u >> (32 - 4 * BLOCK)) << (t + 4 * BLOCK * (g / BLOCK));
-  const uint32_t m = __reduce_max_sync(mask, __float_as_uint(o));       // scores are >= 0: bit order = value order
+  float m = o;
+#pragma unroll
+  for (int s = 4; s < 4 * (BLOCK < 8 ? BLOCK : 8); s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+  if constexpr (BLOCK == 16) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
   const int row = 8 * t + g;
   const bool writer = BLOCK == 16 ? (g == 0 && (t & 1) == 0) : (g % BLOCK) == 0;
-  if (writer && row < rows && cp + row < L) {
-    bmax[(cp + row) / BLOCK] = __uint_as_float(m);
-    atomicAdd(&hist[min(m >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+  if (writer && row < rows) {
+    bmax[blk0 + row / BLOCK] = m;
+    const uint32_t bin = min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1);
+    if (home) atomicAdd(&s_hist[bin], 1u);
+    else atomicAdd(&g_hist[bin], 1u);
   }
 }
 
-template <int BLOCK>
+// Each warp streams a contiguous range of 32-row stages through its own cp.async ring in
+// shared memory (kScanStages stages), so loads in flight hold no registers.  Stages never
+// straddle sequences: sequence b has ceil(len_b / 32) of them and the warps split the
+// concatenated list evenly.  Stage layout: 32 rows x 64 key bytes, then 32 scales stored
+// so that lane quad g finds rows g, g+8, g+16, g+24 in one 16-byte word.
+template <int BLOCK, bool SIGMA, bool PRIV>
 __global__ void __launch_bounds__(kScanWarps * 32, CSA2_SCAN_CTAS) scan_kernel(const __grid_constant__ IdxArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t s_dyn[];
+  static_assert((kScanStages & (kScanStages - 1)) == 0, "ring length must be a power of two");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int B = a.c.B;
-  int64_t *s_units = reinterpret_cast<int64_t *>(s_dyn + kScanSmem);
-  int64_t *s_base = s_units + (B + 1);
+  uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn + kScanSmem);   // PRIV: [kHistBins] home sequence's counts
+  int64_t *s_first = reinterpret_cast<int64_t *>(s_hist + (PRIV ? kHistBins : 0));   // [B + 1] first stage of each sequence
+  int64_t *s_base = s_first + (B + 1);
   int32_t *s_len = reinterpret_cast<int32_t *>(s_base + B);
   for (int i = tid; i < B; i += blockDim.x) {
     SeqTable e = seq_entry(a.c, i, a.max_len, blockIdx.x == 0 ? a.d_err : nullptr);
     s_len[i] = e.len;
     s_base[i] = e.base;
   }
+  if (PRIV)
+    for (int i = tid; i < kHistBins; i += blockDim.x) s_hist[i] = 0u;
   __syncthreads();
-  if (warp == 0) {   // exclusive prefix of 16-position units per sequence
+  if (warp == 0) {   // exclusive prefix of stages per sequence
     const int per = (B + 31) / 32;
     int64_t local = 0;
-    for (int i = lane * per; i < min(B, lane * per + per); ++i) local += (s_len[i] + 15) / 16;
+    for (int i = lane * per; i < min(B, lane * per + per); ++i) local += (s_len[i] + 31) / 32;
     int64_t incl = local;
     for (int o = 1; o < 32; o <<= 1) {
       int64_t v = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += v;
     }
     int64_t run = incl - local;
-    for (int i = lane * per; i < min(B, lane * per + per); ++i) { s_units[i] = run; run += (s_len[i] + 15) / 16; }
-    if (lane == 31) s_units[B] = incl;
+    for (int i = lane * per; i < min(B, lane * per + per); ++i) { s_first[i] = run; run += (s_len[i] + 31) / 32; }
+    if (lane == 31) s_first[B] = incl;
   }
   __syncthreads();
-  const int64_t total = s_units[B];
+  const int64_t total = s_first[B];
   const int64_t W = (int64_t)gridDim.x * kScanWarps;
   const int64_t gw = (int64_t)blockIdx.x * kScanWarps + warp;
-  const int64_t per = (total + W - 1) / W;
-  const int64_t u_begin = min(total, gw * per), u_end = min(total, u_begin + per);
-  if (u_begin >= u_end) return;
+  const int64_t g_begin = total * gw / W, g_end = total * (gw + 1) / W;
+  const int nst = (int)(g_end - g_begin);
   const int g = lane >> 2, t = lane & 3;
-  const uint8_t *ik_codes = a.c.ik_codes;
-  const float *ik_scale = a.c.ik_scale;
-
-  int b0;
-  {
-    int lo = 0, hi = B;                                          // s_units[lo] <= u_begin < s_units[hi]
-    while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (s_units[mid] <= u_begin) lo = mid; else hi = mid; }
-    b0 = lo;
-  }
-  // producer cursor: sequence, next position, units left in this segment / in the warp
-  int pb = b0;
-  int64_t pp = (u_begin - s_units[b0]) * 16;
-  int64_t pleft = u_end - u_begin;
-  int64_t pseg = min(pleft, s_units[b0 + 1] - u_begin);
+  // sequence holding global stage x (skipping empty sequences); x < total
+  auto seq_of = [&](int64_t x) {
+    int lo = 0, hi = B;                                          // s_first[lo] <= x < s_first[hi]
+    while (hi - lo > 1) { int mid = (lo + hi) >> 1; if (s_first[mid] <= x) lo = mid; else hi = mid; }
+    while (s_first[lo + 1] == s_first[lo]) ++lo;
+    return lo;
+  };
+  const int64_t cta_first = total * ((int64_t)blockIdx.x * kScanWarps) / W;
+  const int home_b = PRIV && cta_first < total ? seq_of(cta_first) : -1;  // the CTA's shared histogram counts this one
+  if (nst > 0) {
+  const int b0 = seq_of(g_begin);
   uint8_t *ring = s_dyn + warp * kScanSmemPerWarp;
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
-  uint32_t issued = 0;
+  const uint32_t sc_dst = kStageRows * kDIdx + 4 * ((lane & 7) * 4 + (lane >> 3));
 
-  auto issue_stage = [&]() {
-    const uint32_t dst = ring_s + (issued % kScanStages) * kStageBytes;
-    ++issued;
-    int k = 0;
-    if (pleft > 0) {
-      if (pseg == 0) {                                           // next sequence with work
-        do { ++pb; } while (s_units[pb + 1] == s_units[pb]);
-        pp = 0;
-        pseg = min(pleft, s_units[pb + 1] - s_units[pb]);
+  // producer cursor: sequence, stage within it, its stage count and length, source rows
+  int pb = b0, ps = (int)(g_begin - s_first[b0]);
+  int pn = (int)(s_first[b0 + 1] - s_first[b0]), plen = s_len[b0];
+  const uint8_t *psrc = a.c.ik_codes + (s_base[b0] + 32 * (int64_t)ps) * kDIdx + 16 * t;
+  const float *pscale = a.c.ik_scale + s_base[b0] + 32 * (int64_t)ps + lane;
+  // issue the gathers of this warp's next stage into ring slot k
+  auto issue_stage = [&](int k) {
+    if (ps == pn) {                                              // next sequence with stages
+      do { ++pb; } while (s_first[pb + 1] == s_first[pb]);
+      ps = 0;
+      pn = (int)(s_first[pb + 1] - s_first[pb]);
+      plen = s_len[pb];
+      psrc = a.c.ik_codes + s_base[pb] * kDIdx + 16 * t;
+      pscale = a.c.ik_scale + s_base[pb] + lane;
+    }
+    const uint32_t dst = ring_s + (uint32_t)(k & (kScanStages - 1)) * kStageBytes;
+    const int rows = min(32, plen - 32 * ps);
+    if (rows == 32) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) cp_async16(dst + (g + 8 * q) * kDIdx + 16 * t, psrc + (g + 8 * q) * kDIdx, true);
+      cp_async4(dst + sc_dst, pscale, true);
+    } else {
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const bool v = g + 8 * q < rows;
+        cp_async16(dst + (g + 8 * q) * kDIdx + 16 * t, v ? psrc + (g + 8 * q) * kDIdx : a.c.ik_codes, v);
       }
-      k = (int)min((int64_t)2, pseg);
+      cp_async4(dst + sc_dst, lane < rows ? pscale : a.c.ik_scale, lane < rows);
     }
-    const int64_t L = k ? s_len[pb] : 0;
-    const int64_t base = k ? s_base[pb] : 0;
-    const int lim = (int)min((int64_t)(16 * k), L - pp);            // rows of this stage inside the sequence
-    const uint8_t *src = ik_codes + (base + pp) * kDIdx + 16 * t;
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int r = g + 8 * q;
-      const bool v = r < lim;
-      cp_async16(dst + r * kDIdx + 16 * t, v ? src + r * kDIdx : ik_codes, v);
-    }
-    const bool vs = lane < lim;
-    cp_async4(dst + kStageRows * kDIdx + 4 * ((lane & 7) * 4 + (lane >> 3)), vs ? ik_scale + base + pp + lane : ik_scale,
-              vs);
     cp_async_commit();
-    pp += 16 * k;
-    pseg -= k;
-    pleft -= k;
+    ++ps;
+    psrc += kStageRows * kDIdx;
+    pscale += kStageRows;
   };
-#pragma unroll
-  for (int s = 0; s < kScanStages - 1; ++s) issue_stage();
+  const int pre = min(kScanStages - 1, nst);
+  for (int s = 0; s < pre; ++s) issue_stage(s);
+  for (int s = pre; s < kScanStages - 1; ++s) cp_async_commit();
 
   // consumer cursor mirrors the producer
-  int cb = b0;
-  int64_t cp = (u_begin - s_units[b0]) * 16;
-  int64_t cleft = u_end - u_begin;
-  int64_t cseg = min(cleft, s_units[b0 + 1] - u_begin);
-  uint32_t consumed = 0;
+  int cb = b0, cs = (int)(g_begin - s_first[b0]);
+  int cn = (int)(s_first[b0 + 1] - s_first[b0]), clen = s_len[b0];
   QFrag f;
-  int cur_b = -1;
+  load_qfrag(a.q + (int64_t)cb * kHIdx * kDIdx, a.w + (int64_t)cb * kHIdx, lane, f);
   float smx = 0.f;
-  float *bmax = nullptr;
-  uint32_t *hist = nullptr;
-  int64_t L = 0;
-  while (cleft > 0) {
-    issue_stage();
+  float *bmax = a.ws.bmax + (int64_t)cb * a.ws.nbm;
+  uint32_t *hist = a.ws.hist + (int64_t)cb * kHistBins;
+  bool home = cb == home_b;
+  auto consume = [&](int k) {
     cp_async_wait<kScanStages - 1>();
     __syncwarp();
-    if (cseg == 0) {
-      do { ++cb; } while (s_units[cb + 1] == s_units[cb]);
-      cp = 0;
-      cseg = min(cleft, s_units[cb + 1] - s_units[cb]);
+    if (cs == cn) {                                              // a new sequence: its queries and weights
+      const float m = warp_max(smx);
+      if (lane == 0 && m > 0.f) atomicMax(&a.ws.smax[cb], __float_as_uint(m));
+      do { ++cb; } while (s_first[cb + 1] == s_first[cb]);
+      cs = 0;
+      cn = (int)(s_first[cb + 1] - s_first[cb]);
+      clen = s_len[cb];
+      load_qfrag(a.q + (int64_t)cb * kHIdx * kDIdx, a.w + (int64_t)cb * kHIdx, lane, f);
+      smx = 0.f;
+      bmax = a.ws.bmax + (int64_t)cb * a.ws.nbm;
+      hist = a.ws.hist + (int64_t)cb * kHistBins;
+      home = cb == home_b;
     }
-    const int k = (int)min((int64_t)2, cseg);
-    const uint8_t *st = ring + (consumed % kScanStages) * kStageBytes;
-    ++consumed;
+    const uint8_t *st = ring + (k & (kScanStages - 1)) * kStageBytes;
     const uint4 ka = *reinterpret_cast<const uint4 *>(st + g * kDIdx + 16 * t);
     const uint4 ka8 = *reinterpret_cast<const uint4 *>(st + (g + 8) * kDIdx + 16 * t);
     const uint4 kb = *reinterpret_cast<const uint4 *>(st + (g + 16) * kDIdx + 16 * t);
     const uint4 kb8 = *reinterpret_cast<const uint4 *>(st + (g + 24) * kDIdx + 16 * t);
     const float4 sc = *reinterpret_cast<const float4 *>(st + kStageRows * kDIdx + 16 * g);
     __syncwarp();
-    if (cb != cur_b) {                                           // a new sequence: its queries and weights
-      if (cur_b >= 0) {
-        const float m = warp_max(smx);
-        if (lane == 0) atomicMax(&a.ws.smax[cur_b], __float_as_uint(m));
-      }
-      load_qfrag(a.q + (int64_t)cb * kHIdx * kDIdx, a.w + (int64_t)cb * kHIdx, lane, f);
-      cur_b = cb;
-      smx = 0.f;
-      bmax = a.ws.bmax + (int64_t)cb * a.ws.nbm;
-      hist = a.ws.hist + (int64_t)cb * kHistBins;
-      L = s_len[cb];
-    }
     const float o = score32_row(f, ka, ka8, kb, kb8, sc, t);
     smx = fmaxf(smx, fmaxf(fmaxf(sc.x, sc.y), fmaxf(sc.z, sc.w)));
-    const int row = 8 * t + g;
-    if (a.sigma_out && row < 16 * k && cp + row < L) a.sigma_out[(int64_t)cb * a.max_len + cp + row] = o;
-    emit_stage<BLOCK>(o, lane, cp, 16 * k, L, bmax, hist);
-    cp += 16 * k;
-    cseg -= k;
-    cleft -= k;
+    const int rows = min(32, clen - 32 * cs);
+    if (SIGMA) {
+      const int row = 8 * t + g;
+      if (row < rows) a.sigma_out[(int64_t)cb * a.max_len + 32 * cs + row] = o;
+    }
+    emit_stage<BLOCK>(o, lane, 32 / BLOCK * cs, rows, bmax, s_hist, hist, home);
+    ++cs;
+  };
+  // steady state: every iteration issues one stage and consumes one; then the ring drains
+  int k = 0;
+#pragma unroll 2
+  for (; k + kScanStages - 1 < nst; ++k) {
+    issue_stage(k + kScanStages - 1);
+    consume(k);
+  }
+  for (; k < nst; ++k) {
+    cp_async_commit();
+    consume(k);
   }
   cp_async_wait<0>();
-  if (cur_b >= 0) {
-    const float m = warp_max(smx);
-    if (lane == 0) atomicMax(&a.ws.smax[cur_b], __float_as_uint(m));
+  const float m = warp_max(smx);
+  if (lane == 0 && m > 0.f) atomicMax(&a.ws.smax[cb], __float_as_uint(m));
+  }
+  // the home sequence's counts join the global histogram
+  if (PRIV) __syncthreads();
+  if (PRIV && home_b >= 0) {
+    uint32_t *gh = a.ws.hist + (int64_t)home_b * kHistBins;
+    for (int i = tid; i < kHistBins; i += blockDim.x) {
+      const uint32_t c = s_hist[i];
+      if (c) atomicAdd(&gh[i], c);
+    }
   }
 }
 
@@ -675,6 +696,7 @@ __device__ float hist_threshold_low(const uint32_t *hist_g, int k, int *s_scan, 
 
 template <int BLOCK>
 __global__ void __launch_bounds__(256) collect_kernel(const __grid_constant__ IdxArgs a) {
+  pdl_enter();
   constexpr int kPer = kCollectPer / 256;
   __shared__ int s_scan[8];
   __shared__ int s_misc[4];
@@ -1024,6 +1046,7 @@ __device__ void score_units(const IdxArgs &a, const SeqTable &e, int64_t nb, con
 // come from the scan's histogram of all block maxima.
 template <int BLOCK, bool DIRECT>
 __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __grid_constant__ IdxArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t s_dyn[];
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn);            // radix scratch [2048]
   uint32_t *s_pool_bits = s_hist + 2048;
@@ -1199,6 +1222,7 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
 // for a Reindex layer), many CTAs per sequence, with their histogram.
 template <int BLOCK>
 __global__ void __launch_bounds__(256) score_positions_kernel(const __grid_constant__ IdxArgs a) {
+  pdl_enter();
   const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
@@ -1222,6 +1246,7 @@ __global__ void __launch_bounds__(256) score_positions_kernel(const __grid_const
 // written ascending.  STAGED: the scores fit in shared memory (n_keep * BLOCK <= kStageItems).
 template <int BLOCK, bool STAGED>
 __global__ void __launch_bounds__(kSelCta, 1) select_positions_kernel(const __grid_constant__ IdxArgs a) {
+  pdl_enter();
   extern __shared__ __align__(16) uint8_t s_dyn[];
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn);            // radix scratch [2048]
   uint32_t *s_bits = s_hist + 2048;
@@ -1372,24 +1397,45 @@ int num_sms() {
   return g_num_sms;
 }
 
-static size_t scan_smem_bytes(int B) { return kScanSmem + (size_t)(2 * B + 1) * 8 + (size_t)B * 4; }
+static size_t scan_smem_bytes(int B, bool priv) {
+  return kScanSmem + (priv ? (size_t)kHistBins * 4 : 0) + (size_t)(2 * B + 1) * 8 + (size_t)B * 4;
+}
+
+// Long sequences spread their block maxima over few histogram bins, so that global
+// atomics on the same addresses serialise; there each CTA counts its home sequence in
+// shared memory and adds the counts once at the end.
+static bool scan_private_hist(int64_t max_len) { return max_len >= 262144; }
 
 // persistent scan grid: every resident CTA slot of the GPU, capped by the work
-template <int BLOCK>
+template <int BLOCK, bool PRIV>
 static int scan_grid_size(int B, int64_t max_len) {
   static int per_sm = 0, for_b = -1;
   if (for_b != B) {
-    const size_t smem = scan_smem_bytes(B);
-    cudaFuncSetAttribute(scan_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)scan_smem_bytes(CSA2_MAX_B));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_kernel<BLOCK>, kScanWarps * 32, smem) !=
-            cudaSuccess ||
+    const size_t smem = scan_smem_bytes(B, PRIV);
+    cudaFuncSetAttribute(scan_kernel<BLOCK, false, PRIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)scan_smem_bytes(CSA2_MAX_B, PRIV));
+    cudaFuncSetAttribute(scan_kernel<BLOCK, true, PRIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)scan_smem_bytes(CSA2_MAX_B, PRIV));
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_kernel<BLOCK, false, PRIV>, kScanWarps * 32,
+                                                      smem) != cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     for_b = B;
   }
-  const int64_t units_ub = (int64_t)B * ((max_len + 15) / 16);
-  const int64_t g = std::min<int64_t>((units_ub + kScanWarps - 1) / kScanWarps, (int64_t)num_sms() * per_sm);
+  const int64_t stages_ub = (int64_t)B * ((max_len + 31) / 32);
+  const int64_t g = std::min<int64_t>((stages_ub + kScanWarps - 1) / kScanWarps, (int64_t)num_sms() * per_sm);
   return (int)std::max<int64_t>(g, 1);
+}
+
+template <int BLOCK, bool SIGMA>
+static void launch_scan(IdxArgs &a, int64_t max_len, cudaStream_t st) {
+  const int B = a.c.B;
+  if (scan_private_hist(max_len))
+    launch_k(scan_kernel<BLOCK, SIGMA, true>, dim3(scan_grid_size<BLOCK, true>(B, max_len)), dim3(kScanWarps * 32),
+             scan_smem_bytes(B, true), st, 0, a);
+  else
+    launch_k(scan_kernel<BLOCK, SIGMA, false>, dim3(scan_grid_size<BLOCK, false>(B, max_len)),
+             dim3(kScanWarps * 32), scan_smem_bytes(B, false), st, 0, a);
 }
 
 constexpr size_t kFinalizeSmemDirect =
@@ -1421,32 +1467,31 @@ static int positions_grid(int B) { return std::max(1, std::min(32, (int)((int64_
 template <int BLOCK>
 static void launch_positions(IdxArgs &a, cudaStream_t st) {
   const int B = a.c.B;
-  score_positions_kernel<BLOCK><<<dim3(positions_grid(B), B), 256, 0, st>>>(a);
+  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid(B), B), dim3(256), 0, st, 0, a);
   if ((int64_t)a.n_keep * BLOCK <= kStageItems)
-    select_positions_kernel<BLOCK, true><<<B, kSelCta, kSelectSmemStaged, st>>>(a);
+    launch_k(select_positions_kernel<BLOCK, true>, dim3(B), dim3(kSelCta), kSelectSmemStaged, st, 0, a);
   else
-    select_positions_kernel<BLOCK, false><<<B, kSelCta, kSelectSmemBase, st>>>(a);
+    launch_k(select_positions_kernel<BLOCK, false>, dim3(B), dim3(kSelCta), kSelectSmemBase, st, 0, a);
 }
 
 template <int BLOCK>
 static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_profile *prof, cudaStream_t st) {
   const int B = a.c.B;
   select_smem_optin<BLOCK>();
-  const int scan_grid = scan_grid_size<BLOCK>(B, max_len);
   // inside stream capture a timing event must be an external record node
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   if (prof) cudaStreamIsCapturing(st, &cap);
   const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->start, st, ev_flags);
-  scan_kernel<BLOCK><<<scan_grid, kScanWarps * 32, scan_smem_bytes(B), st>>>(a);
+  launch_scan<BLOCK, false>(a, max_len, st);
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
   const int64_t nbm = a.ws.nbm;
   if (nbm <= kDirectBlocks) {
-    finalize_blocks_kernel<BLOCK, true><<<B, kSelCta, kFinalizeSmemDirect, st>>>(a);
+    launch_k(finalize_blocks_kernel<BLOCK, true>, dim3(B), dim3(kSelCta), kFinalizeSmemDirect, st, 0, a);
   } else {
     dim3 cg((unsigned)((nbm + kCollectPer - 1) / kCollectPer), (unsigned)B);
-    collect_kernel<BLOCK><<<cg, 256, 0, st>>>(a);
-    finalize_blocks_kernel<BLOCK, false><<<B, kSelCta, kFinalizeSmemCand, st>>>(a);
+    launch_k(collect_kernel<BLOCK>, cg, dim3(256), 0, st, 0, a);
+    launch_k(finalize_blocks_kernel<BLOCK, false>, dim3(B), dim3(kSelCta), kFinalizeSmemCand, st, 0, a);
   }
   launch_positions<BLOCK>(a, st);
   return cudaGetLastError();
@@ -1457,6 +1502,20 @@ static cudaError_t reindex_impl(IdxArgs &a, cudaStream_t st) {
   select_smem_optin<BLOCK>();
   launch_positions<BLOCK>(a, st);
   return cudaGetLastError();
+}
+
+// Clears the per-call counters of the workspace (a kernel, so that launches stay chained).
+__global__ void zero_ws_kernel(uint4 *p, int64_t n16) {
+  pdl_enter();
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n16; i += (int64_t)gridDim.x * blockDim.x)
+    p[i] = make_uint4(0, 0, 0, 0);
+}
+
+static cudaError_t zero_ws(const IndexerWs &ws, cudaStream_t st) {
+  const int64_t n16 = (int64_t)(ws.zero_bytes / 16);              // zero_bytes is a multiple of 256
+  const int64_t grid = std::min<int64_t>((n16 + 1023) / 1024, (int64_t)num_sms() * 4);
+  return launch_k(zero_ws_kernel, dim3((unsigned)std::max<int64_t>(grid, 1)), dim3(256), 0, st, 0,
+                  reinterpret_cast<uint4 *>(ws.hist), n16);
 }
 
 static IdxArgs make_args(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len, int n_keep,
@@ -1481,7 +1540,7 @@ static IdxArgs make_args(const csa2_cache &c, const uint16_t *q, const float *w,
 cudaError_t launch_full_select(const csa2_cache &c, const uint16_t *q, const float *w, int block, int n_keep,
                                int topk, int64_t max_len, int32_t *pool, int32_t *topk_idx, const IndexerWs &ws,
                                int32_t *d_err, const csa2_profile *prof, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws.hist, 0, ws.zero_bytes, st);
+  cudaError_t e = zero_ws(ws, st);
   if (e != cudaSuccess) return e;
   IdxArgs a = make_args(c, q, w, max_len, n_keep, topk, ws, d_err);
   a.pool_out = pool;
@@ -1493,7 +1552,7 @@ cudaError_t launch_full_select(const csa2_cache &c, const uint16_t *q, const flo
 cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *pool,
                                   int block, int n_keep, int topk, int64_t max_len, int32_t *topk_idx,
                                   const IndexerWs &ws, int32_t *d_err, cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws.hist, 0, ws.zero_bytes, st);
+  cudaError_t e = zero_ws(ws, st);
   if (e != cudaSuccess) return e;
   IdxArgs a = make_args(c, q, w, max_len, n_keep, topk, ws, d_err);
   a.pool_in = pool;
@@ -1505,12 +1564,12 @@ cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const 
 cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len,
                                float *sigma, double *bound, const IndexerWs &ws, int32_t *d_err,
                                cudaStream_t st) {
-  cudaError_t e = cudaMemsetAsync(ws.hist, 0, ws.zero_bytes, st);
+  cudaError_t e = zero_ws(ws, st);
   if (e != cudaSuccess) return e;
   IdxArgs a = make_args(c, q, w, max_len, 1, 1, ws, d_err);
   a.sigma_out = sigma;
   const int B = c.B;
-  scan_kernel<8><<<scan_grid_size<8>(B, max_len), kScanWarps * 32, scan_smem_bytes(B), st>>>(a);
+  launch_scan<8, true>(a, max_len, st);
   bound_kernel<<<B, 32, 0, st>>>(a, bound);
   return cudaGetLastError();
 }
