@@ -33,7 +33,7 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "decode query-steps/s and achieved HBM GB/s (% of roofline) at 64K and 1M ctx"
-SCAN_BYTES_PER_POS = 68          # 64 FP8 key bytes + 4-byte scale per cached position
+SCAN_BYTES_PER_POS = 72          # per cached position: 64 FP8 key bytes + 4-byte scale read, 4-byte score written
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -142,8 +142,8 @@ def kernels_per_step(wl) -> int:
     from synth.workloads import REINDEX
     n_re = sum(1 for m in wl.schedule if m == REINDEX)
     n_blocks = -(-int(wl.lengths.max()) // wl.block)
-    full = 4 if n_blocks <= 16384 else 5            # scan, [collect,] finalize, score, select
-    return 1 + full + 2 * n_re + wl.n_layers        # append, Full select, Reindex, attention
+    full = 3 if n_blocks <= 16384 else 4            # clear, scan, [collect,] finalize
+    return 1 + full + 3 * n_re + wl.n_layers        # append, Full select, Reindex (clear, score, select), attention
 
 
 def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps: int = 100):

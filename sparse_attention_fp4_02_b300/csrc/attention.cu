@@ -12,8 +12,9 @@
 // first tile is computed.  A tile is dequantised exactly to f16 in shared memory and
 // consumed by mma.sync: S = Q K^T (M = 16 heads), online softmax in f32, O += P V with P
 // split into f16 hi + lo parts (P V error ~2^-22).  Warps merge (m, l, O) through padded
-// shared-memory slices; the CTAs of a cluster then send their partial (m, l, O) into the
-// first CTA's shared memory (distributed shared memory), which merges and writes the row.
+// shared-memory slices; then every CTA of the cluster sends each slice of output dims of
+// its partial O to the CTA that owns those dims, and its (m, l) to all, through
+// distributed shared memory; each CTA merges and writes its dims of the row.
 // Short batches of rows use larger clusters so that the whole GPU takes part.  Nothing is
 // allocated and no CTA waits on a CTA outside its cluster.
 //
@@ -37,7 +38,7 @@ constexpr int kSlot = 2112;           // raw tile: FP4 16 x (64 + 8) = 1,152 B; 
 constexpr int kAttnRing = 4;          // raw tile slots per warp
 constexpr int kOStride = 132;         // floats per merge-slice row
 constexpr int kMaxSplit = 8;           // CTAs per cluster (portable maximum)
-constexpr int kPartFloats = 16 * kD + 32;                           // one CTA's partial: O, m, l
+constexpr int kRecvFloats = 16 * kD + 2 * 16 * kMaxSplit;          // received partial slices + (m, l)
 constexpr int kTileBytes = kTileRows * kStride * 2;                 // 4,352 B
 constexpr int kRingBytes = kAttnRing * kSlot;                       // 8,448 B (= 16 x 132 x 4)
 constexpr float kLog2e = 1.4426950408889634f;
@@ -118,12 +119,25 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, g = lane >> 2, tq = lane & 3;
   uint16_t *tile = reinterpret_cast<uint16_t *>(s_dyn + warp * kTileBytes);
   uint8_t *ring = s_dyn + kAttnWarps * kTileBytes + warp * kRingBytes;
-  float *s_part = reinterpret_cast<float *>(s_dyn + kAttnWarps * (kTileBytes + kRingBytes));   // [split][kPartFloats]
+  // received partials: O slices [split][16][128 / split], then m [split][16], l [split][16]
+  float *s_recv = reinterpret_cast<float *>(s_dyn + kAttnWarps * (kTileBytes + kRingBytes));
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   // every CTA of the cluster has started before any writes into another's shared memory
   if (split > 1) cluster_arrive_relaxed();
 
-  // ---- the query row and its sequence
+  // ---- the query row, its sequence and this warp's first indices, loaded together
+  const int slots = split * kAttnWarps, slot_id = crank * kAttnWarps + warp;
+  const int n_tiles_max = a.tiles_sel + a.tiles_win;
+  const int tw0 = (int)((int64_t)n_tiles_max * slot_id / slots);
+  const int tw1_max = (int)((int64_t)n_tiles_max * (slot_id + 1) / slots);
+  const int r = lane >> 1, hf = lane & 1;
+  const int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
+  int32_t idx_pre[kAttnRing];
+#pragma unroll
+  for (int s = 0; s < kAttnRing; ++s) {
+    const int ti = tw0 + s, j = ti * kTileRows + r;
+    idx_pre[s] = (ti < tw1_max && ti < a.tiles_sel && j < a.topk) ? __ldg(idx_row + j) : -1;
+  }
   const int b = a.q_seq[t];
   const int64_t p = a.q_pos[t];
   bool ok = b >= 0 && b < a.c.B;
@@ -137,25 +151,21 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     set_err(a.d_err, (b < 0 || b >= a.c.B) ? CSA2_DEVERR_SEQ : CSA2_DEVERR_POS);
 
   // ---- queries (bf16 -> f16 into shared memory); their loads overlap the first gathers
-  uint4 qv = make_uint4(0, 0, 0, 0);
-  if (tid < 256) {                                            // 16 heads x 16 chunks of 8 values
-    const int h = tid >> 4, c8 = tid & 15;
-    qv = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8));
+  constexpr int kQPer = 256 / (kAttnWarps * 32);                    // 16 heads x 16 chunks of 8 values
+  uint4 qv[kQPer];
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int i = tid + j * kAttnWarps * 32, h = i >> 4, c8 = i & 15;
+    qv[j] = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8));
   }
 
   // ---- this warp's tiles: the row's tiles are split evenly over every warp of the cluster
-  const int n_tiles = ok ? a.tiles_sel + a.tiles_win : 0;
-  const int slots = split * kAttnWarps, slot_id = crank * kAttnWarps + warp;
-  const int tw0 = (int)((int64_t)n_tiles * slot_id / slots), tw1 = (int)((int64_t)n_tiles * (slot_id + 1) / slots);
+  const int tw1 = ok ? tw1_max : tw0;
   const int swa_ring = a.swa.ring;
-  const int r = lane >> 1, hf = lane & 1;
-  const int32_t *idx_row = a.topk_idx + (int64_t)t * a.topk;
-  auto issue = [&](int ti, int slot) {
+  auto issue = [&](int ti, int slot, int32_t idx) {
     const uint32_t dst = ring_s + slot * kSlot;
     bool valid = false;
     if (ti < a.tiles_sel) {
-      const int j = ti * kTileRows + r;
-      const int32_t idx = j < a.topk ? __ldg(idx_row + j) : -1;
       if (idx >= 0) {
         if (idx > p) { if (hf == 0) set_err(a.d_err, CSA2_DEVERR_INDEX); }
         else valid = true;
@@ -181,15 +191,16 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
   };
 #pragma unroll
   for (int s = 0; s < kAttnRing; ++s) {
-    if (tw0 + s < tw1) issue(tw0 + s, s);
+    if (tw0 + s < tw1) issue(tw0 + s, s, idx_pre[s]);
     else cp_async_commit();
   }
-  if (tid < 256) {
-    const int h = tid >> 4, c8 = tid & 15;
-    const uint32_t w[4] = {qv.x, qv.y, qv.z, qv.w};
+#pragma unroll
+  for (int j = 0; j < kQPer; ++j) {
+    const int i = tid + j * kAttnWarps * 32, h = i >> 4, c8 = i & 15;
+    const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
     uint32_t o4[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o4[j] = pack_f16x2(bf16_to_f32(w[j] & 0xFFFFu), bf16_to_f32(w[j] >> 16));
+    for (int k = 0; k < 4; ++k) o4[k] = pack_f16x2(bf16_to_f32(w[k] & 0xFFFFu), bf16_to_f32(w[k] >> 16));
     sts128(s_q + h * kStride + 8 * c8, o4[0], o4[1], o4[2], o4[3]);
   }
   __syncthreads();
@@ -249,8 +260,12 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     if (hf == 0) { s_rs[warp][r] = rs; s_vs[warp][r] = vs; }
     __syncwarp();
     // the slot is free again: start the gather of a later tile into it
-    if (tw0 + i + kAttnRing < tw1) issue(tw0 + i + kAttnRing, slot);
-    else cp_async_commit();
+    if (tw0 + i + kAttnRing < tw1) {
+      const int ti = tw0 + i + kAttnRing, j = ti * kTileRows + r;
+      issue(ti, slot, ti < a.tiles_sel && j < a.topk ? __ldg(idx_row + j) : -1);
+    } else {
+      cp_async_commit();
+    }
 
     // ---- S = Q K^T over the 16 rows (two n-tiles of 8 rows)
     float sc[2][4];
@@ -383,9 +398,11 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     if (a.lse && tid < 16) a.lse[head0 + tid] = s_cl[tid] > 0.f ? s_cm[tid] + logf(s_cl[tid]) : -INFINITY;
     return;
   }
-  // ---- cluster merge: every CTA sends (O, m, l) into slot crank of the first CTA
+  // ---- cluster merge: CTA q owns output dims [q * dw, (q + 1) * dw); every CTA sends it
+  // that slice of its partial O and sends its (m, l) to every CTA
+  const int dw = kD / split;
   cluster_wait_acquire();                                      // every CTA of the cluster is running
-  const uint32_t slot0 = map_to_rank((uint32_t)__cvta_generic_to_shared(s_part + crank * kPartFloats), 0);
+  const uint32_t recv_s = (uint32_t)__cvta_generic_to_shared(s_recv);
   for (int i = tid; i < 16 * 32; i += blockDim.x) {
     const int h = i >> 5, d4 = (i & 31) * 4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -394,57 +411,63 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
       const float4 v = *reinterpret_cast<const float4 *>(rings + w * kRingBytes + (h * kOStride + d4) * 4);
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
-    st_cluster_v4(slot0 + (h * kD + d4) * 4, acc);
+    const int owner = d4 / dw;
+    st_cluster_v4(map_to_rank(recv_s + ((crank * 16 + h) * dw + (d4 - owner * dw)) * 4, (uint32_t)owner), acc);
   }
-  if (tid < 16) {
-    st_cluster_f32(slot0 + (16 * kD + tid) * 4, s_cm[tid]);
-    st_cluster_f32(slot0 + (16 * kD + 16 + tid) * 4, s_cl[tid]);
+  for (int i = tid; i < 16 * split; i += blockDim.x) {
+    const int owner = i >> 4, h = i & 15;
+    const uint32_t at = map_to_rank(recv_s + (16 * kD + crank * 16 + h) * 4, (uint32_t)owner);
+    st_cluster_f32(at, s_cm[h]);
+    st_cluster_f32(at + 16 * kMaxSplit * 4, s_cl[h]);
   }
   cluster_arrive_release();
   cluster_wait_acquire();
-  if (crank != 0) return;
+  const float *rm = s_recv + 16 * kD, *rl = rm + 16 * kMaxSplit;
   if (tid < 16) {
     float M = -INFINITY, L = 0.f;
-    for (int q = 0; q < split; ++q) M = fmaxf(M, s_part[q * kPartFloats + 16 * kD + tid]);
+    for (int q = 0; q < split; ++q) M = fmaxf(M, rm[q * 16 + tid]);
     for (int q = 0; q < split; ++q) {
-      const float mq = s_part[q * kPartFloats + 16 * kD + tid];
-      const float f = mq == -INFINITY ? 0.f : exp2f((mq - M) * kLog2e);
-      s_part[q * kPartFloats + 16 * kD + tid] = f;            // the partial's weight
-      L += s_part[q * kPartFloats + 16 * kD + 16 + tid] * f;
+      const float mq = rm[q * 16 + tid];
+      L += mq == -INFINITY ? 0.f : rl[q * 16 + tid] * exp2f((mq - M) * kLog2e);
     }
     s_cm[tid] = M;
     s_cl[tid] = L;
   }
   __syncthreads();
-  for (int i = tid; i < 16 * 32; i += blockDim.x) {
-    const int h = i >> 5, d4 = (i & 31) * 4;
+  for (int i = tid; i < 16 * (dw / 4); i += blockDim.x) {
+    const int h = i / (dw / 4), d4 = (i % (dw / 4)) * 4;
+    const float M = s_cm[h];
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int q = 0; q < split; ++q) {
-      const float f = s_part[q * kPartFloats + 16 * kD + h];
-      const float4 v = *reinterpret_cast<const float4 *>(s_part + q * kPartFloats + h * kD + d4);
+      const float mq = rm[q * 16 + h];
+      const float f = mq == -INFINITY ? 0.f : exp2f((mq - M) * kLog2e);
+      const float4 v = *reinterpret_cast<const float4 *>(s_recv + (q * 16 + h) * dw + d4);
       acc.x += v.x * f; acc.y += v.y * f; acc.z += v.z * f; acc.w += v.w * f;
     }
     const float l = s_cl[h];
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    *reinterpret_cast<float4 *>(a.out + (head0 + h) * kD + d4) =
+    *reinterpret_cast<float4 *>(a.out + (head0 + h) * kD + crank * dw + d4) =
         make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
   }
-  if (a.lse && tid < 16) a.lse[head0 + tid] = s_cl[tid] > 0.f ? s_cm[tid] + logf(s_cl[tid]) : -INFINITY;
+  if (crank == 0 && a.lse && tid < 16) a.lse[head0 + tid] = s_cl[tid] > 0.f ? s_cm[tid] + logf(s_cl[tid]) : -INFINITY;
 }
 
 // ------------------------------------------------------------------ host side
 
 static size_t attn_smem(int split) {
-  return (size_t)kAttnWarps * (kTileBytes + kRingBytes) + (split > 1 ? (size_t)split * kPartFloats * 4 : 0);
+  return (size_t)kAttnWarps * (kTileBytes + kRingBytes) + (split > 1 ? (size_t)kRecvFloats * 4 : 0);
 }
 
 size_t attn_ws_bytes(int64_t, int32_t, int32_t, int32_t) { return 0; }
 
 // CTAs per cluster: the largest power of two (<= 8) that keeps every (row, head group)
-// cluster resident at once, one CTA per SM.
+// cluster resident at once (CSA2_ATTN_CTAS_PER_SM CTAs per SM).
+#ifndef CSA2_ATTN_CTAS_PER_SM
+#define CSA2_ATTN_CTAS_PER_SM 1
+#endif
 static int attn_split(int64_t rows) {
   int split = 1;
-  while (split < kMaxSplit && rows * split * 2 <= (int64_t)num_sms()) split *= 2;
+  while (split < kMaxSplit && rows * split * 2 <= CSA2_ATTN_CTAS_PER_SM * (int64_t)num_sms()) split *= 2;
   return split;
 }
 

@@ -402,7 +402,8 @@ struct IdxArgs {
   int32_t *pool_out;        // [B][n_keep]
   const int32_t *pool_in;   // Reindex: [B][n_keep]
   int32_t *topk_out;        // [B][topk]
-  float *sigma_out;         // test: [B][max_len]
+  float *sigma_out;         // scan's position scores [B][sigma_stride]
+  int64_t sigma_stride;
   int32_t *d_err;
   int32_t use_pool;         // position stage reads pool_in instead of the candidate list
 };
@@ -496,7 +497,8 @@ __device__ __forceinline__ void emit_stage(float o, int lane, int blk0, int rows
 // concatenated list evenly.  Stage layout: 32 rows x 64 key bytes, then 32 scales stored
 // so that lane quad g finds rows g, g+8, g+16, g+24 in one 16-byte word.
 template <int BLOCK, bool SIGMA, bool PRIV>
-__global__ void __launch_bounds__(kScanWarps * 32, CSA2_SCAN_CTAS) scan_kernel(const __grid_constant__ IdxArgs a) {
+__global__ void __launch_bounds__(kScanWarps * 32, PRIV ? 2 : CSA2_SCAN_CTAS)
+    scan_kernel(const __grid_constant__ IdxArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t s_dyn[];
   static_assert((kScanStages & (kScanStages - 1)) == 0, "ring length must be a power of two");
@@ -624,7 +626,7 @@ __global__ void __launch_bounds__(kScanWarps * 32, CSA2_SCAN_CTAS) scan_kernel(c
     const int rows = min(32, clen - 32 * cs);
     if (SIGMA) {
       const int row = 8 * t + g;
-      if (row < rows) a.sigma_out[(int64_t)cb * a.max_len + 32 * cs + row] = o;
+      if (row < rows) a.sigma_out[(int64_t)cb * a.sigma_stride + 32 * cs + row] = o;
     }
     emit_stage<BLOCK>(o, lane, 32 / BLOCK * cs, rows, bmax, s_hist, hist, home);
     ++cs;
@@ -1036,12 +1038,65 @@ __device__ void score_units(const IdxArgs &a, const SeqTable &e, int64_t nb, con
   }
 }
 
+// Shared tail of the position selections: items [0, n) with approximate scores val(i)
+// (-1 invalid), n_valid of them valid, the topk-th largest in histogram bin `bin`.
+// Writes the exact top-k positions ascending to out (-1 padded).  Every thread calls it.
+struct PosWork {
+  uint32_t *radix;     // [2048] radix scratch
+  uint32_t *bits;      // item bitmap, ceil(n / 32) words
+  int32_t *m, *band;   // [kListCap]
+  float2 *ex;          // [kListCap]
+  const int32_t *lut;  // [256]
+  int *cnt, *scan, *out;
+  int (*wc)[4];
+  int *tot;
+};
+
+template <int BLOCK, class ValFn, class PosFn>
+__device__ void select_positions_core(const IdxArgs &a, const SeqTable &e, int b, int n, int n_valid, uint32_t bin,
+                                      ValFn val, PosFn pos_of, float E, const PosWork &w, int32_t *out) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
+  const float *wb = a.w + (int64_t)b * kHIdx;
+  auto id = [](int i) -> int32_t { return i; };                      // item order = position order
+  auto pick = [&](int i) { atomicOr(&w.bits[i >> 5], 1u << (i & 31)); };
+  auto cert = [&](int word, int, unsigned c1, unsigned) { if (lane == 0) w.bits[word] = c1; };
+  int32_t *g_m = a.ws.unc_id + (int64_t)b * 3 * a.ws.unc_x;
+  if (n_valid <= a.topk) {
+    // every valid score is selected: "certain" = valid, nothing near
+    classify_words(n, val, true, 1.f, -0.5f, false, 0.f, 0.f, cert, NearLists{w.m, w.m, g_m, g_m}, w.wc, w.tot);
+  } else {
+    const float w_hi = hi_cut(bin_hi(bin), E), w_lo = lo_cut(bin_lo(bin), E);
+    classify_words(n, val, true, w_lo, w_hi, false, 0.f, 0.f, cert, NearLists{w.m, w.m, g_m, g_m}, w.wc, w.tot);
+    const int mc = w.tot[0], n_cert = w.tot[2];
+    const bool big = mc > kListCap;
+    const int32_t *m = big ? g_m : w.m;
+    int32_t *band = big ? g_m + a.ws.unc_x : w.band;
+    float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : w.ex;
+    auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
+      QExact q;
+      load_qexact(qb, wb, lane, q);
+      for (int j = warp; j < u; j += kSelWarps) {
+        const int64_t row = e.base + pos_of(bd[j]);
+        const uint4 kk = __ldg(reinterpret_cast<const uint4 *>(a.c.ik_codes + row * kDIdx + 16 * (lane & 3)));
+        const float2 v = exact_sigma(q, kk, __ldg(a.c.ik_scale + row), w.lut);
+        if (lane == 0) xv[j] = v;
+      }
+    };
+    resolve_list(m, mc, a.topk, n_cert, w_lo, w_hi, E, val, id, exact_band, pick, band, ex, w.radix, w.cnt, w.scan,
+                 w.out);
+  }
+  __syncthreads();
+  emit_bits_ascending(w.bits, (n + 31) / 32, pos_of, out, a.topk, w.scan);
+}
+
 // ---- the Full layer after the scan: pool + position-candidate blocks
 
+// The Full layer's selection after the scan, one CTA per sequence.
 // Pool = the top min(n_keep, nb) blocks by (exact block score desc, id asc), ascending.
 // Position-candidate blocks = every block whose approximate maximum reaches the lower cut
-// of the topk-th largest approximate block maximum (they contain every top-k position),
-// ascending.  DIRECT: the sequence's block maxima are the items (nb <= kDirectBlocks);
+// of the topk-th largest approximate block maximum (they contain every top-k position);
+// their positions, with the scores the scan stored, give the exact top-k positions.  DIRECT: the sequence's block maxima are the items (nb <= kDirectBlocks);
 // otherwise the items are the candidates gathered by collect_kernel.  Both thresholds
 // come from the scan's histogram of all block maxima.
 template <int BLOCK, bool DIRECT>
@@ -1054,7 +1109,8 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
   int32_t *s_m1 = reinterpret_cast<int32_t *>(s_pcb_bits + kIdWords);
   int32_t *s_m2 = s_m1 + kListCap;
   int32_t *s_band = s_m2 + kListCap;
-  float2 *s_ex = reinterpret_cast<float2 *>(s_band + kListCap);
+  int32_t *s_band2 = s_band + kListCap;
+  float2 *s_ex = reinterpret_cast<float2 *>(s_band2 + kListCap);
   int32_t *s_lut = reinterpret_cast<int32_t *>(s_ex + kListCap);
   float *s_val = reinterpret_cast<float *>(s_lut + 256);
   int32_t *s_id = reinterpret_cast<int32_t *>(s_val + kStageItems);  // candidate mode only
@@ -1072,7 +1128,6 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
   const int k1 = min(n_keep, nb), k2 = min(a.topk, nb);
   const bool sel_pool = nb > n_keep, sel_pcb = nb > a.topk;
   int32_t *pool = a.pool_out + (int64_t)b * n_keep;
-  int32_t *pcb = a.ws.pcb + (int64_t)b * n_keep;
   const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
   const float *wb = a.w + (int64_t)b * kHIdx;
   const uint32_t *hist_g = a.ws.hist + (int64_t)b * kHistBins;
@@ -1195,10 +1250,12 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
     for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < k1 ? s_sort[i] : -1;
   }
   __syncthreads();
-  int n_pcb;
+  // ---- the candidate blocks, ascending, into shared memory
+  int32_t *s_list = s_m1;                                          // m1 + m2: 2 kListCap >= kMaxSel ids
+  int count;
   if (!sel_pcb) {
-    for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = i < nb ? i : -1;
-    n_pcb = nb;
+    for (int i = tid; i < nb; i += blockDim.x) s_list[i] = i;
+    count = nb;
   } else {
     int cnt = 0;
     if (use_bits)
@@ -1206,16 +1263,50 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
     cnt = __reduce_add_sync(0xffffffffu, cnt);
     if (lane == 0) atomicAdd(&s_cnt[kCntPcb], cnt);
     __syncthreads();
-    n_pcb = s_cnt[kCntPcb];
+    const int n_pcb = s_cnt[kCntPcb];
     if (!use_bits || n_pcb > n_keep) {
-      // the pool contains every top-k position's block and is already ascending
-      for (int i = tid; i < n_keep; i += blockDim.x) pcb[i] = pool[i];
-      n_pcb = k1;
+      // the pool contains every top-k position's block
+      if (!sel_pool) for (int i = tid; i < nb; i += blockDim.x) s_list[i] = i;
+      else if (use_bits) emit_bits_ascending(s_pool_bits, nwords, [](int i) { return (int32_t)i; }, s_list, n_keep, s_scan);
+      else for (int i = tid; i < k1; i += blockDim.x) s_list[i] = s_sort[i];
+      count = k1;
     } else {
-      emit_bits_ascending(s_pcb_bits, nwords, [](int i) { return (int32_t)i; }, pcb, n_keep, s_scan);
+      emit_bits_ascending(s_pcb_bits, nwords, [](int i) { return (int32_t)i; }, s_list, n_keep, s_scan);
+      count = n_pcb;
     }
   }
-  if (tid == 0) a.ws.pcb_cnt[b] = (uint32_t)n_pcb;
+  __syncthreads();
+
+  // ---- their positions, with the scan's scores: histogram, then the exact top-k
+  const int np = count * BLOCK;
+  const bool pstaged = np <= kStageItems;
+  uint32_t *s_phist = s_pool_bits;                                  // [kHistBins]
+  uint32_t *s_ibits = s_pcb_bits;                                   // item bitmap
+  for (int i = tid; i < kHistBins; i += blockDim.x) s_phist[i] = 0u;
+  __syncthreads();
+  const float *sig = a.sigma_out + (int64_t)b * a.sigma_stride;
+  auto pos_of = [&](int i) -> int32_t { return s_list[i / BLOCK] * BLOCK + (i % BLOCK); };
+  auto pval = [&](int i) -> float {
+    const int32_t pos = pos_of(i);
+    return pos < e.len ? __ldcg(sig + pos) : -1.f;
+  };
+  for (int i0 = tid; i0 < np; i0 += 4 * blockDim.x) {
+    float v[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) { const int i = i0 + j * blockDim.x; v[j] = i < np ? pval(i) : -1.f; }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int i = i0 + j * blockDim.x;
+      if (pstaged && i < np) s_val[i] = v[j];
+      if (v[j] >= 0.f) atomicAdd(&s_phist[min(__float_as_uint(v[j]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+    }
+  }
+  __syncthreads();
+  cta_find_bins(a.topk, 0, [&](int bin) { return s_phist[bin]; }, s_scan, s_out);
+  auto pv = [&](int i) -> float { return pstaged ? s_val[i] : pval(i); };
+  const PosWork w{s_hist, s_ibits, s_band, s_band2, s_ex, s_lut, s_cnt, s_scan, s_out, s_wc, s_tot};
+  select_positions_core<BLOCK>(a, e, b, np, s_out[4], (uint32_t)s_out[0], pv, pos_of, E, w,
+                               a.topk_out + (int64_t)b * a.topk);
 }
 
 // Scores of the positions of a block list (the Full layer's candidate blocks, or the pool
@@ -1270,7 +1361,6 @@ __global__ void __launch_bounds__(kSelCta, 1) select_positions_kernel(const __gr
   if (a.use_pool) { list_g = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
   else { list_g = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
   const int n = count * BLOCK;
-  const int nwords = (n + 31) / 32;
   const float *pv_g = a.ws.pvals + (int64_t)b * a.ws.pv_stride;     // 16-byte aligned rows
   const uint16_t *qb = a.q + (int64_t)b * kHIdx * kDIdx;
   const float *wb = a.w + (int64_t)b * kHIdx;
@@ -1297,38 +1387,10 @@ __global__ void __launch_bounds__(kSelCta, 1) select_positions_kernel(const __gr
     for (int i = tid + 1; i < count; i += blockDim.x)
       if (s_list[i] >= 0 && s_list[i - 1] >= s_list[i]) set_err(a.d_err, CSA2_DEVERR_POOL);
   auto val = [&](int i) -> float { return STAGED ? s_pv[i] : __ldcg(pv_g + i); };
-  auto id = [](int i) -> int32_t { return i; };                      // item order = position order
-  auto pick = [&](int i) { atomicOr(&s_bits[i >> 5], 1u << (i & 31)); };
   auto pos_of = [&](int i) -> int32_t { return s_list[i / BLOCK] * BLOCK + (i % BLOCK); };
-  auto cert = [&](int w, int, unsigned c1, unsigned) { if (lane == 0) s_bits[w] = c1; };
-  int32_t *g_m = a.ws.unc_id + (int64_t)b * 3 * a.ws.unc_x;
-  if (n_valid <= a.topk) {
-    // every valid score is selected: "certain" = valid, nothing near
-    classify_words(n, val, true, 1.f, -0.5f, false, 0.f, 0.f, cert, NearLists{s_m, s_m, g_m, g_m}, s_wc, s_tot);
-  } else {
-    const uint32_t bin = (uint32_t)s_out[0];
-    const float w_hi = hi_cut(bin_hi(bin), E), w_lo = lo_cut(bin_lo(bin), E);
-    classify_words(n, val, true, w_lo, w_hi, false, 0.f, 0.f, cert, NearLists{s_m, s_m, g_m, g_m}, s_wc, s_tot);
-    const int mc = s_tot[0], n_cert = s_tot[2];
-    const bool big = mc > kListCap;
-    const int32_t *m = big ? g_m : s_m;
-    int32_t *band = big ? g_m + a.ws.unc_x : s_band;
-    float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : s_ex;
-    auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
-      QExact q;
-      load_qexact(qb, wb, lane, q);
-      for (int j = warp; j < u; j += kSelWarps) {
-        const int64_t row = e.base + pos_of(bd[j]);
-        const uint4 kk = __ldg(reinterpret_cast<const uint4 *>(a.c.ik_codes + row * kDIdx + 16 * (lane & 3)));
-        const float2 v = exact_sigma(q, kk, __ldg(a.c.ik_scale + row), s_lut);
-        if (lane == 0) xv[j] = v;
-      }
-    };
-    resolve_list(m, mc, a.topk, n_cert, w_lo, w_hi, E, val, id, exact_band, pick, band, ex, s_hist, s_cnt, s_scan,
-                 s_out);
-  }
-  __syncthreads();
-  emit_bits_ascending(s_bits, nwords, pos_of, a.topk_out + (int64_t)b * a.topk, a.topk, s_scan);
+  const PosWork w{s_hist, s_bits, s_m, s_band, s_ex, s_lut, s_cnt, s_scan, s_out, s_wc, s_tot};
+  select_positions_core<BLOCK>(a, e, b, n, n_valid, (uint32_t)s_out[0], val, pos_of, E, w,
+                               a.topk_out + (int64_t)b * a.topk);
 }
 
 // ------------------------------------------------------------------ test: bounds
@@ -1357,6 +1419,7 @@ size_t indexer_ws_bytes(int32_t B, int64_t max_len, int32_t block, int32_t n_kee
   s += align_up((size_t)B * nbm * 8);       // cand
   s += align_up((size_t)B * n_keep * 4);    // pcb
   s += align_up((size_t)B * npos * 4);      // pvals
+  s += align_up((size_t)B * nbm * block * 4);   // sigma
   s += align_up((size_t)B * unc * 12);      // unc_id: three lists per sequence
   s += align_up((size_t)B * unc * 8);       // unc_val
   return s;
@@ -1381,6 +1444,8 @@ IndexerWs indexer_ws_carve(void *ws, int32_t B, int64_t max_len, int32_t block, 
   w.cand = (uint64_t *)p; p += align_up((size_t)B * nbm * 8);
   w.pcb = (int32_t *)p; p += align_up((size_t)B * n_keep * 4);
   w.pvals = (float *)p; p += align_up((size_t)B * npos * 4);
+  w.sigma = (float *)p; p += align_up((size_t)B * nbm * block * 4);
+  w.sigma_stride = nbm * block;
   w.unc_id = (int32_t *)p; p += align_up((size_t)B * w.unc_x * 12);
   w.unc_val = (float2 *)p;
   return w;
@@ -1439,7 +1504,7 @@ static void launch_scan(IdxArgs &a, int64_t max_len, cudaStream_t st) {
 }
 
 constexpr size_t kFinalizeSmemDirect =
-    (size_t)(2048 + 2 * kIdWords) * 4 + (size_t)3 * kListCap * 4 + (size_t)kListCap * 8 + 256 * 4 +
+    (size_t)(2048 + 2 * kIdWords) * 4 + (size_t)4 * kListCap * 4 + (size_t)kListCap * 8 + 256 * 4 +
     (size_t)kStageItems * 4;
 constexpr size_t kFinalizeSmemCand = kFinalizeSmemDirect + (size_t)kStageItems * 4;
 constexpr size_t kSelectSmemBase = (size_t)(2048 + kItemWords) * 4 + (size_t)2 * kListCap * 4 +
@@ -1483,7 +1548,7 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
   if (prof) cudaStreamIsCapturing(st, &cap);
   const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->start, st, ev_flags);
-  launch_scan<BLOCK, false>(a, max_len, st);
+  launch_scan<BLOCK, true>(a, max_len, st);
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
   const int64_t nbm = a.ws.nbm;
   if (nbm <= kDirectBlocks) {
@@ -1493,7 +1558,6 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
     launch_k(collect_kernel<BLOCK>, cg, dim3(256), 0, st, 0, a);
     launch_k(finalize_blocks_kernel<BLOCK, false>, dim3(B), dim3(kSelCta), kFinalizeSmemCand, st, 0, a);
   }
-  launch_positions<BLOCK>(a, st);
   return cudaGetLastError();
 }
 
@@ -1522,7 +1586,8 @@ static IdxArgs make_args(const csa2_cache &c, const uint16_t *q, const float *w,
                          int topk, const IndexerWs &ws, int32_t *d_err) {
   IdxArgs a;
   a.c = c; a.q = q; a.w = w; a.max_len = max_len; a.n_keep = n_keep; a.topk = topk; a.ws = ws;
-  a.pool_out = nullptr; a.pool_in = nullptr; a.topk_out = nullptr; a.sigma_out = nullptr;
+  a.pool_out = nullptr; a.pool_in = nullptr; a.topk_out = nullptr;
+  a.sigma_out = ws.sigma; a.sigma_stride = ws.sigma_stride;
   a.d_err = d_err; a.use_pool = 0;
   return a;
 }
@@ -1568,6 +1633,7 @@ cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const flo
   if (e != cudaSuccess) return e;
   IdxArgs a = make_args(c, q, w, max_len, 1, 1, ws, d_err);
   a.sigma_out = sigma;
+  a.sigma_stride = max_len;
   const int B = c.B;
   launch_scan<8, true>(a, max_len, st);
   bound_kernel<<<B, 32, 0, st>>>(a, bound);

@@ -28,11 +28,13 @@ struct IndexerWs {           // carved out of the caller's workspace
   float *bmax;               // [B][nbm]
   uint64_t *cand;            // [B][nbm]
   int32_t *pcb;              // [B][n_keep]
-  float *pvals;              // [B][pv_stride] position scores
+  float *pvals;              // [B][pv_stride] position scores (Reindex)
+  float *sigma;              // [B][sigma_stride] the scan's position scores (Full)
   int32_t *unc_id;           // [B][3][unc_x] item lists that overflow shared memory
   float2 *unc_val;           // [B][unc_x] their exact scores as normalised double-floats
   int64_t nbm, unc_x;        // block maxima per sequence (a multiple of 4), overflow list length
   int64_t pv_stride;         // n_keep * block rounded up to a multiple of 4
+  int64_t sigma_stride;      // nbm * block
   size_t zero_bytes;         // bytes at the start that must be zeroed per call
 };
 
