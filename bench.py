@@ -34,6 +34,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode query-steps/s and achieved HBM GB/s (% of roofline) at 64K and 1M ctx"
 SCAN_BYTES_PER_POS = 72          # per cached position: 64 FP8 key bytes + 4-byte scale read, 4-byte score written
+FALLBACK_BF16_TFLOPS = 1800.0
 FALLBACK_HBM_GBS = 6400.0
 
 
@@ -44,6 +45,17 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def peaks_tensor():
+    """Dense f16/bf16 tensor peak in TFLOP/s (f16 runs at the bf16 rate): the measured cuBLAS
+    burst figure, for a kernel timed on its own."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops"]), "measured"
+    return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 # ------------------------------------------------------------------ clocks
@@ -231,6 +243,34 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
     return res
 
 
+def measure_chunked(iters: int = 20, warmup: int = 3):
+    """The chunked-query attention workload (4,096 query rows, 64 heads, 262,144-token cache):
+    one sparse_attn_decode call per iteration, device-timed; inputs (229 MB) exceed L2."""
+    import torch
+    from sparse_attention_fp4_02_b300.runner import ChunkedRunner
+    from synth.workloads import config
+
+    r = ChunkedRunner(config(3))
+    for _ in range(warmup):
+        r.step()
+    torch.cuda.synchronize()
+    r.check_device_errors()
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for _ in range(iters):
+        r.step()
+    t1.record()
+    torch.cuda.synchronize()
+    r.check_device_errors()
+    us = t0.elapsed_time(t1) / iters * 1e3
+    res = {"workload": r.wl.name, "us_per_call": us, "tflops": r.flops() / (us * 1e-6) / 1e12,
+           "gbs": r.bytes() / (us * 1e-6) / 1e9, "flops_per_call": r.flops(), "bytes_per_call": r.bytes(),
+           "iters": iters}
+    del r
+    torch.cuda.empty_cache()
+    return res
+
+
 def blas_threads() -> int:
     """Threads the oracle's numpy/BLAS calls use on this host."""
     try:
@@ -272,6 +312,7 @@ def run_ours(args, world, rank, local):
     res1m = None
     if not args.no_1m and args.config != 2:
         res1m = measure_workload(2, max(1, args.steps // 2), args.warmup, world)
+    resq = None if args.no_chunked else measure_chunked()
     clocks = clock.stop()
     if rank != 0:
         return
@@ -305,6 +346,10 @@ def run_ours(args, world, rank, local):
                           "ms_per_step": res1m["ms_per_step"], "steps": res1m["steps"],
                           "scan_us": res1m["scan_ms"] * 1e3, "scan_gbs": a2, "scan_frac": a2 / peak,
                           "e2e": res1m["e2e"]["value"], "gpu_launches": res1m["launches"]}
+    if resq:
+        tpeak = peaks_tensor()
+        line["chunked"] = dict(resq, bound="tensor", peak_tflops=tpeak[0], peak_source=tpeak[1],
+                               tensor_frac=resq["tflops"] / tpeak[0])
     if not args.no_cpu:
         line["cpu_baseline"] = cpu_baseline(args.config)
     print(json.dumps(line), flush=True)
@@ -352,6 +397,7 @@ def main():
     ap.add_argument("--config", type=int, default=1, choices=[0, 1, 2, 4])
     ap.add_argument("--no-1m", action="store_true", help="skip the 1M-context workload")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-query attention workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

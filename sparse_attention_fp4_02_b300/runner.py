@@ -169,3 +169,71 @@ class DecodeRunner:
         with torch.cuda.graph(g):
             self.step(prof)
         return g
+
+
+class ChunkedRunner:
+    """The chunked-query workload: many consecutive query rows of one sequence, each with
+    its own causal top-k plus a causal window, attended in one sparse_attn_decode call."""
+
+    def __init__(self, wl, device="cuda", chunk: int = 1 << 17):
+        from synth.workloads import ChunkedWorkload
+        assert isinstance(wl, ChunkedWorkload)
+        self.wl, self.device = wl, device
+        L, s = int(wl.cache_len), wl.seed
+        self.cache = Cache(((L + 15) // 16) * 16, 1, device)
+        self.cache.seq_base.zero_()
+        self.cache.seq_len.fill_(L)
+        self.swa = SwaRing(1, wl.ring, device)
+        cos, sin = synth.rope_table(L + 1)
+        self.rope_cos, self.rope_sin = _to_dev(cos, torch.float32, device), _to_dev(sin, torch.float32, device)
+        self.d_err = torch.zeros(1, dtype=torch.int32, device=device)
+        oc = synth.outlier_channels(s, synth.Stream.KV_OUTLIER)
+        soc = synth.outlier_channels(s, synth.Stream.SWA_OUTLIER)
+        for lo in range(0, L, chunk):
+            hi = min(L, lo + chunk)
+            pos = np.arange(lo, hi, dtype=np.int64)
+            rows = synth.row_id(0, pos)
+            kv = _bf16_dev(synth.normals_bf16(s, synth.Stream.KV, 0, rows, 128, oc), device)
+            ik = _bf16_dev(synth.normals_bf16(s, synth.Stream.IK, 0, rows, 64), device)
+            sid = torch.zeros(hi - lo, dtype=torch.int32, device=device)
+            kv_append_fp4(self.cache, None, kv, ik, None, self.rope_cos, self.rope_sin, sid,
+                          torch.from_numpy(pos).to(device), self.d_err)
+        # window rows of every query: positions [first query - window + 1, L)
+        lo = max(0, L - wl.n_query - wl.window + 1)
+        pos = np.arange(lo, L, dtype=np.int64)
+        rows = synth.row_id(0, pos)
+        kv = _bf16_dev(synth.normals_bf16(s, synth.Stream.KV, 0, rows, 128, oc), device)
+        sw = _bf16_dev(synth.normals_bf16(s, synth.Stream.SWA, 0, rows, 128, soc)[None], device)
+        kv_append_fp4(self.cache, [self.swa], kv, None, sw, self.rope_cos, self.rope_sin,
+                      torch.zeros(L - lo, dtype=torch.int32, device=device), torch.from_numpy(pos).to(device),
+                      self.d_err)
+        q_pos = np.arange(L - wl.n_query, L, dtype=np.int64)
+        self.q_pos = torch.from_numpy(q_pos).to(device)
+        self.q_seq = torch.zeros(wl.n_query, dtype=torch.int32, device=device)
+        self.topk = torch.from_numpy(synth.causal_topk(s, q_pos, wl.topk)).to(device)
+        q = synth.normals_bf16(s, synth.Stream.Q, 0, np.arange(wl.n_query * wl.H), 128)
+        self.q = _bf16_dev(q.reshape(wl.n_query, wl.H, 128), device)
+        self.out = torch.empty((wl.n_query, wl.H, 128), dtype=torch.float32, device=device)
+        self.lse = torch.empty((wl.n_query, wl.H), dtype=torch.float32, device=device)
+        self.ws = alloc_workspace(0, device)
+        self.tau = 1.0 / math.sqrt(128.0)
+        torch.cuda.synchronize()
+
+    def step(self):
+        sparse_attn_decode(self.cache, self.swa, self.q, self.q_seq, self.q_pos, self.topk, self.wl.window,
+                           self.tau, self.out, self.lse, self.ws, self.d_err)
+
+    def flops(self) -> float:
+        """Dense-equivalent flops of one call: S = Q K^T and O = P V over topk + window rows."""
+        wl = self.wl
+        return 4.0 * wl.n_query * wl.H * (wl.topk + wl.window) * 128
+
+    def bytes(self) -> int:
+        """Algorithmic bytes of one call: gathered FP4 rows, FP8 window rows, indices, q, o."""
+        wl = self.wl
+        return wl.n_query * (wl.topk * 72 + wl.window * 132 + 4 * wl.topk + 2 * wl.H * 128 + 4 * wl.H * 128)
+
+    def check_device_errors(self):
+        v = int(self.d_err.item())
+        if v:
+            raise RuntimeError(f"device error bits 0x{v:x}")
