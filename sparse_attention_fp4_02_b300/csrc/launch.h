@@ -59,6 +59,12 @@ cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const u
                                int topk, int window, float tau, float *out, float *lse, void *ws,
                                int32_t *d_err, cudaStream_t st);
 
+// chunked-query attention on tcgen05 (many rows, H <= 64)
+bool attn_tc_eligible(int64_t T, int H);
+cudaError_t launch_attn_chunked_tc(const csa2_cache &c, const csa2_swa &swa, const uint16_t *q, int H, int64_t T,
+                                   const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx, int topk,
+                                   int window, float tau, float *out, float *lse, int32_t *d_err, cudaStream_t st);
+
 int num_sms();
 
 }  // namespace csa2

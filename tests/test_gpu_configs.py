@@ -83,7 +83,7 @@ def test_config4_ragged_b64_twenty_layers():
 
 
 def test_config3_chunked_queries_h64_cache262144():
-    from tests.test_gpu_attention import World
+    from tests.test_gpu_attention import LSE_TOL_TC, World
     wl = config(3)
     w = World([wl.cache_len], ring=wl.ring)
     q_pos = np.arange(wl.cache_len - wl.n_query, wl.cache_len, dtype=np.int64)
@@ -95,7 +95,7 @@ def test_config3_chunked_queries_h64_cache262144():
     ref, rlse = w.oracle(q[rows], np.zeros(len(rows), np.int32), q_pos[rows], topk[rows], wl.window)
     e = attn_rel_err(out[rows], ref)
     assert e <= ATTN_TOL, e
-    assert np.max(np.abs(lse[rows] - rlse)) <= 1e-4
+    assert np.max(np.abs(lse[rows] - rlse)) <= LSE_TOL_TC      # many rows: the tensor-core path
     # every row's output is a convex combination: finite, and lse finite
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
     print("max rel err", e)
