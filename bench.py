@@ -171,15 +171,17 @@ def kernels_per_step(wl) -> int:
     n_re = sum(1 for m in wl.schedule if m == REINDEX)
     n_blocks = -(-int(wl.lengths.max()) // wl.block)
     full = 3 if n_blocks <= 16384 else 4            # clear, scan, [collect,] finalize
+    if wl.drafts > 1:                               # every indexer layer also runs the verify rows' selection
+        n_re += 1
     return 1 + full + 3 * n_re + wl.n_layers        # append, Full select, Reindex (clear, score, select), attention
 
 
-def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps: int = 100):
+def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int = 100):
     import torch
     from sparse_attention_fp4_02_b300.runner import DecodeRunner
     from synth.workloads import config
 
-    wl = config(cfg)
+    wl = config(cfg) if isinstance(cfg, int) else cfg
     r = DecodeRunner(wl)
     r.build_cache()
     G = max(1, min(graph_steps, steps))
@@ -222,6 +224,9 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
             (pin(r.h_swa_new.view(np.int16)), r.swa_new), (pin(r.h_q.view(np.int16)), r.q)]
     h_in += [(pin(r.h_qidx[l].view(np.int16)), r.qidx[l]) for l in r.idx_layers]
     h_in += [(pin(r.h_w[l]), r.w[l]) for l in r.idx_layers]
+    if r.D > 1:                  # the Full layer's own copy of each session's last row
+        h_in += [(pin(r.h_qidx[l][r.D - 1::r.D].view(np.int16)), r.qidx_last[l]) for l in r.full_layers]
+        h_in += [(pin(r.h_w[l][r.D - 1::r.D]), r.w_last[l]) for l in r.full_layers]
     h_out = [torch.empty(r.out.shape, dtype=torch.float32).pin_memory(),
              torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()]
     h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
@@ -248,9 +253,9 @@ def measure_workload(cfg: int, steps: int, warmup: int, world: int, graph_steps:
     r.check_device_errors()
 
     res = {
-        "wl": wl, "steps": steps, "ms": ms, "ms_per_step": ms / steps, "value": aggregate_rate(wl.B * steps, world, ms),
+        "wl": wl, "steps": steps, "ms": ms, "ms_per_step": ms / steps, "value": aggregate_rate(r.T * steps, world, ms),
         "scan_ms": scan_ms, "scan_bytes": SCAN_BYTES_PER_POS * int(wl.lengths.sum()),
-        "e2e": {"value": aggregate_rate(wl.B * n_e2e, world, e2e_ms), "unit": "query-steps/s",
+        "e2e": {"value": aggregate_rate(r.T * n_e2e, world, e2e_ms), "unit": "query-steps/s",
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e},
         "launches": kernels_per_step(wl) * steps,
     }
@@ -329,6 +334,10 @@ def run_ours(args, world, rank, local):
     if not args.no_1m and args.config != 2:
         res1m = measure_workload(2, max(1, args.steps // 2), args.warmup, world)
     resq = None if args.no_chunked else measure_chunked()
+    resv = None
+    if not args.no_verify:
+        from synth.workloads import verify_workload
+        resv = measure_workload(verify_workload(), max(1, args.steps // 2), args.warmup, world)
     clocks = clock.stop()
     if rank != 0:
         return
@@ -362,6 +371,16 @@ def run_ours(args, world, rank, local):
                           "ms_per_step": res1m["ms_per_step"], "steps": res1m["steps"],
                           "scan_us": res1m["scan_ms"] * 1e3, "scan_gbs": a2, "scan_frac": a2 / peak,
                           "e2e": res1m["e2e"]["value"], "gpu_launches": res1m["launches"]}
+    if resv:
+        w3 = resv["wl"]
+        a3 = resv["scan_bytes"] / (resv["scan_ms"] / 1e3) / 1e9
+        line["verify"] = {"workload": w3.name, "value": resv["value"], "unit": "verified-rows/s",
+                          "rows_per_step": w3.B * w3.drafts, "ms_per_step": resv["ms_per_step"],
+                          "steps": resv["steps"], "scan_us": resv["scan_ms"] * 1e3, "scan_gbs": a3,
+                          "scan_frac": a3 / peak, "e2e": resv["e2e"]["value"],
+                          "h2d_bytes_per_step": resv["e2e"]["h2d_bytes_per_step"],
+                          "d2h_bytes_per_step": resv["e2e"]["d2h_bytes_per_step"],
+                          "gpu_launches": resv["launches"]}
     if resq:
         tpeak = peaks_tensor()
         line["chunked"] = dict(resq, bound="tensor", peak_tflops=tpeak[0], peak_source=tpeak[1],
@@ -414,6 +433,7 @@ def main():
     ap.add_argument("--no-1m", action="store_true", help="skip the 1M-context workload")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--no-chunked", action="store_true", help="skip the chunked-query attention workload")
+    ap.add_argument("--no-verify", action="store_true", help="skip the draft-verification workload")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -119,7 +119,8 @@ typedef struct csa2_profile {
 enum csa2_op {
   CSA2_OP_FULL_SELECT = 1,
   CSA2_OP_REINDEX_SELECT = 2,
-  CSA2_OP_ATTN_DECODE = 3
+  CSA2_OP_ATTN_DECODE = 3,
+  CSA2_OP_VERIFY_SELECT = 4
 };
 
 /* Human-readable name of a status code (static string). */
@@ -129,6 +130,7 @@ const char *csa2_status_string(int status);
  * Workspace bytes needed by one call of `op` (written to *bytes).
  *   FULL_SELECT / REINDEX_SELECT: B, max_len, block, n_keep_blocks, topk used.
  *   ATTN_DECODE: T (query rows), H (heads), topk, window used.
+ *   VERIFY_SELECT: T (query rows), block, n_keep_blocks, topk used.
  * Returns CSA2_ERR_INVALID_ARG for out-of-range sizes.  Workspace must be
  * 256-byte aligned; its contents need not be initialised and are clobbered.
  */
@@ -160,6 +162,24 @@ int kv_append_fp4(const csa2_cache *cache, const csa2_swa *swa_layers, int32_t n
                   const float *rope_cos, const float *rope_sin, int64_t rope_len,
                   const int32_t *seq_id, const int64_t *pos, int64_t n, int32_t *d_err,
                   csa2_stream_t stream);
+
+/*
+ * swa_refill_fp8 - rebuild the sliding-window rings of every layer from replayed
+ * window KV, leaving the global cache untouched.
+ * (origotech.dev deep dive, subsection "FP4와 SWA Bounded Replay": the FP8 window
+ * KV is not persisted; after a restart the last window of tokens is replayed and
+ * its per-layer KV re-appended)
+ *   swa_layers     host array of n_swa_layers (1..CSA2_MAX_SWA_LAYERS) ring descriptors
+ *   B              number of sequences (seq_id must lie in [0, B))
+ *   swa_new        bf16 [n_swa_layers][n][128] replayed window KV before RoPE
+ *   rope_cos/sin, seq_id, pos, n, d_err: as kv_append_fp4
+ * Each token's vector of each layer is rotated and quantised exactly as
+ * kv_append_fp4 does for its SWA layers (same bytes) into slot pos % ring.
+ * Tokens with a bad seq_id or position are skipped (CSA2_DEVERR_SEQ / _POS).
+ */
+int swa_refill_fp8(const csa2_swa *swa_layers, int32_t n_swa_layers, int32_t B, const uint16_t *swa_new,
+                   const float *rope_cos, const float *rope_sin, int64_t rope_len, const int32_t *seq_id,
+                   const int64_t *pos, int64_t n, int32_t *d_err, csa2_stream_t stream);
 
 /*
  * indexer_full_select - a Full layer's indexer over every cached position.
@@ -230,6 +250,33 @@ int indexer_reindex_select_static(const csa2_cache *cache, const uint16_t *q_idx
                                   const int32_t *pool_blocks, int32_t block, int32_t n_keep_blocks,
                                   int32_t topk, int64_t max_len, int32_t *topk_idx, int32_t *d_err,
                                   csa2_stream_t stream);
+
+/*
+ * indexer_verify_select - the Reindex selection for several query rows per session,
+ * each with its own indexer queries and a causal limit: the rows verifying a batch
+ * of drafted positions in speculative decoding.
+ * (origotech.dev deep dive, section "아키텍처는 어떻게 KV 캐시를 줄이나", the DSpark
+ * item of the remaining stack: a drafter proposes 5 positions at once, which are then
+ * verified; the selection itself is the Reindex rule of subsection "Compressed Sparse
+ * Attention 2(CSA2)")
+ *   q_idx          bf16 [T][8][64] indexer queries of each row
+ *   w              float [T][8]    head weights of each row
+ *   q_seq, q_pos   int32 [T], int64 [T]: session and position of each row
+ *   T              rows, 0..65535
+ *   pool_blocks    int32 [B][n_keep_blocks] each session's pool (shared by its rows),
+ *                  ascending, -1 entries ignored
+ *   topk_idx       int32 [T][topk] out: the min(topk, candidates) best positions
+ *                  p' <= q_pos[r] among the pool's positions, by (score desc,
+ *                  position asc), ascending, -1 padded
+ *   ws/ws_bytes    csa2_workspace_bytes(CSA2_OP_VERIFY_SELECT, ...)
+ * Other arguments as indexer_reindex_select.  A row with a bad q_seq or q_pos
+ * selects nothing and sets CSA2_DEVERR_SEQ / _POS; a pool id beyond its session's
+ * length sets CSA2_DEVERR_POOL; pool positions after q_pos are not candidates.
+ */
+int indexer_verify_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                          const int64_t *q_pos, int64_t T, const int32_t *pool_blocks, int32_t block,
+                          int32_t n_keep_blocks, int32_t topk, int64_t max_len, int32_t *topk_idx, void *ws,
+                          size_t ws_bytes, int32_t *d_err, csa2_stream_t stream);
 
 /*
  * sparse_attn_decode - gathered FP4 dequantisation fused into sparse attention.

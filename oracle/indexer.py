@@ -97,6 +97,20 @@ def reindex_select(q_bf16, w, ik_codes, ik_scale, pool, block=8, topk=512):
     return pad(top_k_ids(sigma, pos, topk), topk), sigma, pos
 
 
+def verify_select(q_bf16, w, ik_codes, ik_scale, pool, p: int, block=8, topk=512):
+    """One verify row at position p: top-k over the session's pool positions p' <= p.
+
+    Speculative decoding (origotech.dev deep dive, section "아키텍처는 어떻게 KV 캐시를
+    줄이나", the DSpark item) checks several drafted positions at once; each such row
+    ranks the pool its session's Full layer kept, under the row's own indexer queries,
+    and sees only the positions up to its own (the causal limit).
+    """
+    pos = pool_positions(pool, ik_codes.shape[0], block)
+    pos = pos[pos <= p]
+    sigma = scores(q_bf16, w, ik_codes[pos], ik_scale[pos])
+    return pad(top_k_ids(sigma, pos, topk), topk), sigma, pos
+
+
 def reuse(topk_idx):
     """Reuse layer: the indices are passed on unchanged."""
     return topk_idx

@@ -6,8 +6,8 @@ library's CUDA kernels.  PyTorch provides device memory and streams.  If the
 library has not been built, importing this package raises: there is no CPU
 fallback.
 
-Entry points (same names as the C ABI): ``kv_append_fp4``,
-``indexer_full_select``, ``indexer_reindex_select``, ``sparse_attn_decode``,
+Entry points (same names as the C ABI): ``kv_append_fp4``, ``swa_refill_fp8``,
+``indexer_full_select``, ``indexer_reindex_select``, ``indexer_verify_select``, ``sparse_attn_decode``,
 plus ``workspace_bytes`` and the ``Cache`` / ``SwaRing`` containers that own
 the device tensors of the layouts the header documents.
 """
@@ -28,7 +28,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID_ARG, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
 DEVERR_SEQ, DEVERR_POS, DEVERR_LEN, DEVERR_INDEX, DEVERR_POOL, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
-OP_FULL_SELECT, OP_REINDEX_SELECT, OP_ATTN_DECODE = 1, 2, 3
+OP_FULL_SELECT, OP_REINDEX_SELECT, OP_ATTN_DECODE, OP_VERIFY_SELECT = 1, 2, 3, 4
 D, D_IDX, H_IDX = 128, 64, 8
 MAX_SWA_LAYERS = 32
 
@@ -63,17 +63,20 @@ _lib.csa2_status_string.restype = ctypes.c_char_p
 _ws_bytes = _sig("csa2_workspace_bytes", [ctypes.c_int, _I32, _I64, _I32, _I32, _I32, _I64, _I32, _I32,
                                           ctypes.POINTER(_SZ)])
 _append = _sig("kv_append_fp4", [_P, _P, _I32, _P, _P, _P, _P, _P, _I64, _P, _P, _I64, _P, _P])
+_refill = _sig("swa_refill_fp8", [_P, _I32, _I32, _P, _P, _P, _I64, _P, _P, _I64, _P, _P])
 _full = _sig("indexer_full_select", [_P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P, _SZ, _P, _P, _P])
 _reindex = _sig("indexer_reindex_select", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _SZ, _P, _P])
 _reindex_static = _sig("indexer_reindex_select_static", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P])
+_verify = _sig("indexer_verify_select", [_P, _P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I64, _P, _P, _SZ, _P,
+                                         _P])
 _attn = _sig("sparse_attn_decode", [_P, _P, _P, _I32, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P, _P, _SZ,
                                     _P, _P])
 _t_fp4 = _sig("csa2_test_quantize_fp4", [_P, _I64, _P, _P, _P])
 _t_fp8 = _sig("csa2_test_quantize_fp8", [_P, _I64, _I32, _P, _P, _P])
 _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _P, _P])
 
-EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "indexer_full_select",
-            "indexer_reindex_select", "indexer_reindex_select_static", "sparse_attn_decode", "csa2_test_quantize_fp4",
+EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "swa_refill_fp8", "indexer_full_select",
+            "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
             "csa2_test_quantize_fp8", "csa2_test_index_scores")
 
 
@@ -154,6 +157,14 @@ def kv_append_fp4(cache: Cache, swa_layers, kv_new, ik_new, swa_new, rope_cos, r
                    _ptr(d_err), _stream(stream)), "kv_append_fp4")
 
 
+def swa_refill_fp8(swa_layers, B, swa_new, rope_cos, rope_sin, seq_id, pos, d_err, stream=None):
+    """Re-append replayed window KV into every layer's FP8 ring (the global cache is not touched)."""
+    layers = list(swa_layers)
+    arr = (SwaDesc * len(layers))(*[s.desc() for s in layers])
+    _check(_refill(arr, len(layers), int(B), _ptr(swa_new), _ptr(rope_cos), _ptr(rope_sin), int(rope_cos.shape[0]),
+                   _ptr(seq_id), _ptr(pos), int(seq_id.shape[0]), _ptr(d_err), _stream(stream)), "swa_refill_fp8")
+
+
 def indexer_full_select(cache: Cache, q_idx, w, block, n_keep_blocks, topk, max_len, pool_blocks, topk_idx, ws,
                         d_err, prof=None, stream=None):
     pd = None
@@ -177,6 +188,14 @@ def indexer_reindex_select_static(cache: Cache, q_idx, w, pool_blocks, block, n_
     _check(_reindex_static(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(pool_blocks), block,
                            n_keep_blocks, topk, int(max_len), _ptr(topk_idx), _ptr(d_err), _stream(stream)),
            "indexer_reindex_select_static")
+
+
+def indexer_verify_select(cache: Cache, q_idx, w, q_seq, q_pos, pool_blocks, block, n_keep_blocks, topk, max_len,
+                          topk_idx, ws, d_err, stream=None):
+    """Per query row (session q_seq, position q_pos): top-k over the session's pool, causally limited."""
+    _check(_verify(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(q_seq), _ptr(q_pos), int(q_seq.shape[0]),
+                   _ptr(pool_blocks), block, n_keep_blocks, topk, int(max_len), _ptr(topk_idx), _ptr(ws), ws.numel(),
+                   _ptr(d_err), _stream(stream)), "indexer_verify_select")
 
 
 def sparse_attn_decode(cache: Cache, swa: SwaRing, q, q_seq, q_pos, topk_idx, window, softmax_scale, out, lse, ws,

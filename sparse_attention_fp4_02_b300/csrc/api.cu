@@ -75,6 +75,10 @@ int csa2_workspace_bytes(int op, int32_t B, int64_t max_len, int32_t block, int3
       if (!select_sizes_ok(B, max_len, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
       *bytes = indexer_ws_bytes(B, max_len, block, n_keep_blocks);
       return CSA2_OK;
+    case CSA2_OP_VERIFY_SELECT:
+      if (T < 0 || T > 65535 || !select_sizes_ok(1, 0, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
+      *bytes = indexer_ws_bytes((int32_t)(T > 0 ? T : 1), 0, block, n_keep_blocks);
+      return CSA2_OK;
     case CSA2_OP_ATTN_DECODE:
       if (!attn_sizes_ok(T, H, topk, window)) return CSA2_ERR_INVALID_ARG;
       *bytes = attn_ws_bytes(T, H, topk, window);
@@ -109,6 +113,27 @@ int kv_append_fp4(const csa2_cache *cache, const csa2_swa *swa_layers, int32_t n
                                    rope_cos, rope_sin, rope_len, seq_id, pos, n, d_err, (cudaStream_t)stream));
 }
 
+int swa_refill_fp8(const csa2_swa *swa_layers, int32_t n_swa_layers, int32_t B, const uint16_t *swa_new,
+                   const float *rope_cos, const float *rope_sin, int64_t rope_len, const int32_t *seq_id,
+                   const int64_t *pos, int64_t n, int32_t *d_err, csa2_stream_t stream) {
+  if (n < 0 || !d_err || B < 1 || B > CSA2_MAX_B) return CSA2_ERR_INVALID_ARG;
+  if (n_swa_layers < 1 || n_swa_layers > CSA2_MAX_SWA_LAYERS || !swa_layers) return CSA2_ERR_INVALID_ARG;
+  for (int l = 0; l < n_swa_layers; ++l) {
+    const csa2_swa &w = swa_layers[l];
+    if (!w.codes || !w.scale || w.ring < 1 || !aligned(w.codes, 16) || !aligned(w.scale, 4))
+      return CSA2_ERR_INVALID_ARG;
+  }
+  if (n > 0 && (!swa_new || !aligned(swa_new, 8) || !rope_cos || !rope_sin || rope_len < 1 || !seq_id || !pos))
+    return CSA2_ERR_INVALID_ARG;
+  int st = device_ok();
+  if (st != CSA2_OK) return st;
+  csa2_cache none;
+  std::memset(&none, 0, sizeof(none));
+  none.B = B;                                                // sequence ids are checked against B only
+  return cuda_status(launch_append(none, swa_layers, n_swa_layers, nullptr, nullptr, swa_new, rope_cos, rope_sin,
+                                   rope_len, seq_id, pos, n, d_err, (cudaStream_t)stream));
+}
+
 int indexer_full_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, int32_t block,
                         int32_t n_keep_blocks, int32_t topk, int64_t max_len, int32_t *pool_blocks,
                         int32_t *topk_idx, void *ws, size_t ws_bytes, int32_t *d_err, const csa2_profile *prof,
@@ -141,6 +166,24 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
   IndexerWs iw = indexer_ws_carve(ws, cache->B, max_len, block, n_keep_blocks);
   return cuda_status(launch_reindex_select(*cache, q_idx, w, pool_blocks, block, n_keep_blocks, topk, max_len,
                                            topk_idx, iw, d_err, (cudaStream_t)stream));
+}
+
+int indexer_verify_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                          const int64_t *q_pos, int64_t T, const int32_t *pool_blocks, int32_t block,
+                          int32_t n_keep_blocks, int32_t topk, int64_t max_len, int32_t *topk_idx, void *ws,
+                          size_t ws_bytes, int32_t *d_err, csa2_stream_t stream) {
+  if (!cache_ok(cache) || !d_err || T < 0 || T > 65535) return CSA2_ERR_INVALID_ARG;
+  if (!select_sizes_ok(cache->B, max_len, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!q_idx || !aligned(q_idx, 16) || !w || !aligned(w, 4) || !q_seq || !q_pos || !pool_blocks || !topk_idx)
+    return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < indexer_ws_bytes((int32_t)T, 0, block, n_keep_blocks))
+    return CSA2_ERR_WORKSPACE;
+  int st = device_ok();
+  if (st != CSA2_OK) return st;
+  IndexerWs iw = indexer_ws_carve(ws, (int32_t)T, 0, block, n_keep_blocks);
+  return cuda_status(launch_verify_select(*cache, q_idx, w, q_seq, q_pos, T, pool_blocks, block, n_keep_blocks, topk,
+                                          max_len, topk_idx, iw, d_err, (cudaStream_t)stream));
 }
 
 int sparse_attn_decode(const csa2_cache *cache, const csa2_swa *swa, const uint16_t *q, int32_t H, int64_t T,

@@ -52,6 +52,7 @@ struct AppendArgs {
   const int32_t *seq_id;
   const int64_t *pos;
   int64_t n;
+  int32_t main_part;       // 1: part 0 writes the main KV (+ indexer key); 0: window rings only
   int32_t *d_err;
 };
 
@@ -66,10 +67,10 @@ __device__ __forceinline__ void load4_bf16(const uint16_t *p, float x[4]) {
 __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ AppendArgs a) {
   pdl_enter();
   const int lane = threadIdx.x & 31;
-  const int parts = a.swa_new ? 1 + a.n_swa : 1;
+  const int parts = (a.swa_new ? a.n_swa : 0) + a.main_part;
   const int64_t wid = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int64_t tok = wid / parts;
-  const int part = (int)(wid - tok * parts);
+  const int part = (int)(wid - tok * parts) + 1 - a.main_part;   // 0 = main KV, 1 + l = window layer l
   if (tok >= a.n) return;
   // independent loads first: the token's identity and this part's input row
   const int b = __ldg(a.seq_id + tok);
@@ -99,8 +100,8 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
   if (lane >= 16) { rotate(x[0], x[1], c0, s0); rotate(x[2], x[3], c1, s1); }
 
   // a token whose cache row is out of range is skipped by every part
-  const int64_t row = a.c.seq_base[b] + p;
-  if (row < 0 || row >= a.c.T_cap) {
+  const int64_t row = a.main_part ? a.c.seq_base[b] + p : 0;
+  if (a.main_part && (row < 0 || row >= a.c.T_cap)) {
     if (lane == 0) set_err(a.d_err, CSA2_DEVERR_POS);
     return;
   }
@@ -145,8 +146,10 @@ cudaError_t launch_append(const csa2_cache &c, const csa2_swa *swa, int n_swa, c
   a.kv_new = kv_new; a.ik_new = ik_new; a.swa_new = swa_new;
   a.cos = cos; a.sin = sin; a.rope_len = rope_len;
   a.seq_id = seq_id; a.pos = pos; a.n = n; a.d_err = d_err;
+  a.main_part = kv_new ? 1 : 0;
   const int warps = 8;
-  const int64_t parts = swa_new ? 1 + n_swa : 1;
+  const int64_t parts = (swa_new ? n_swa : 0) + a.main_part;
+  if (parts == 0) return cudaSuccess;
   const int64_t grid = (n * parts + warps - 1) / warps;
   return launch_k(kv_append_kernel, dim3((unsigned)grid), dim3(warps * 32), 0, st, 0, a);
 }

@@ -406,7 +406,51 @@ struct IdxArgs {
   int64_t sigma_stride;
   int32_t *d_err;
   int32_t use_pool;         // position stage reads pool_in instead of the candidate list
+  const int32_t *row_seq;   // verify rows: [rows] session of each query row (null: one row per sequence)
+  const int64_t *row_pos;   // verify rows: [rows] position of each query row (causal limit)
 };
+
+// One unit of the position stage: a sequence, or (verify rows) one query row of a session.
+// q, w, workspace slices and outputs are indexed by r; the pool and the keys by b; positions
+// at or beyond e.len are not candidates (the causal limit of a verify row); nb_seq counts the
+// whole sequence's blocks (pool ids beyond it are errors).
+struct SelUnit {
+  int r, b;
+  SeqTable e;
+  int64_t nb_seq;
+};
+
+template <int BLOCK>
+__device__ __forceinline__ SelUnit sel_unit(const IdxArgs &a, int r) {
+  SelUnit u;
+  u.r = r;
+  if (!a.row_seq) {
+    u.b = r;
+    u.e = seq_entry(a.c, r, a.max_len, nullptr);
+    u.nb_seq = (u.e.len + BLOCK - 1) / BLOCK;
+    return u;
+  }
+  const int b = a.row_seq[r];
+  const int64_t p = a.row_pos[r];
+  if (b < 0 || b >= a.c.B) {
+    if (threadIdx.x == 0) set_err(a.d_err, CSA2_DEVERR_SEQ);
+    u.b = 0;
+    u.e.len = 0;
+    u.e.base = 0;
+    u.nb_seq = 0;
+    return u;
+  }
+  u.b = b;
+  u.e = seq_entry(a.c, b, a.max_len, nullptr);
+  u.nb_seq = (u.e.len + BLOCK - 1) / BLOCK;
+  if (p < 0 || p >= u.e.len) {
+    if (threadIdx.x == 0) set_err(a.d_err, CSA2_DEVERR_POS);
+    u.e.len = 0;
+  } else {
+    u.e.len = (int32_t)(p + 1);
+  }
+  return u;
+}
 
 // ------------------------------------------------------------------ scan
 
@@ -1314,23 +1358,22 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
 template <int BLOCK>
 __global__ void __launch_bounds__(256) score_positions_kernel(const __grid_constant__ IdxArgs a) {
   pdl_enter();
-  const int b = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
-  const int64_t nb = (e.len + BLOCK - 1) / BLOCK;
+  const SelUnit u = sel_unit<BLOCK>(a, blockIdx.y);
+  const int r = u.r;
   const int32_t *list;
   int count;
-  if (a.use_pool) { list = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
-  else { list = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
+  if (a.use_pool) { list = a.pool_in + (int64_t)u.b * a.n_keep; count = a.n_keep; }
+  else { list = a.ws.pcb + (int64_t)r * a.n_keep; count = (int)a.ws.pcb_cnt[r]; }
   const int n = count * BLOCK;
-  float *pv = a.ws.pvals + (int64_t)b * a.ws.pv_stride;
+  float *pv = a.ws.pvals + (int64_t)r * a.ws.pv_stride;
   QFrag f;
-  load_qfrag(a.q + (int64_t)b * kHIdx * kDIdx, a.w + (int64_t)b * kHIdx, lane, f);
+  load_qfrag(a.q + (int64_t)r * kHIdx * kDIdx, a.w + (int64_t)r * kHIdx, lane, f);
   float smx = 0.f;
-  score_units<BLOCK>(a, e, nb, list, n, pv, a.ws.hist2 + (int64_t)b * kHistBins, f, blockIdx.x * 8 + warp,
+  score_units<BLOCK>(a, u.e, u.nb_seq, list, n, pv, a.ws.hist2 + (int64_t)r * kHistBins, f, blockIdx.x * 8 + warp,
                      gridDim.x * 8, smx);
   smx = warp_max(smx);
-  if (lane == 0 && smx > 0.f) atomicMax(&a.ws.smax2[b], __float_as_uint(smx));
+  if (lane == 0 && smx > 0.f) atomicMax(&a.ws.smax2[r], __float_as_uint(smx));
 }
 
 // Exact top-k over the scored positions (the Full layer's candidates, or a Reindex pool),
@@ -1353,12 +1396,13 @@ __global__ void __launch_bounds__(kSelCta, 1) select_positions_kernel(const __gr
   __shared__ int s_wc[kSelWarps][4];
   __shared__ int s_tot[4];
   __shared__ float s_E;
-  const int b = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const SeqTable e = seq_entry(a.c, b, a.max_len, nullptr);
+  const SelUnit u = sel_unit<BLOCK>(a, blockIdx.x);
+  const int b = u.r;                                                 // q, w, workspace and output slot
+  const SeqTable e = u.e;
   const int32_t *list_g;
   int count;
-  if (a.use_pool) { list_g = a.pool_in + (int64_t)b * a.n_keep; count = a.n_keep; }
+  if (a.use_pool) { list_g = a.pool_in + (int64_t)u.b * a.n_keep; count = a.n_keep; }
   else { list_g = a.ws.pcb + (int64_t)b * a.n_keep; count = (int)a.ws.pcb_cnt[b]; }
   const int n = count * BLOCK;
   const float *pv_g = a.ws.pvals + (int64_t)b * a.ws.pv_stride;     // 16-byte aligned rows
@@ -1562,6 +1606,17 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
 }
 
 template <int BLOCK>
+static cudaError_t verify_impl(IdxArgs &a, int rows, cudaStream_t st) {
+  select_smem_optin<BLOCK>();
+  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid(rows), rows), dim3(256), 0, st, 0, a);
+  if ((int64_t)a.n_keep * BLOCK <= kStageItems)
+    launch_k(select_positions_kernel<BLOCK, true>, dim3(rows), dim3(kSelCta), kSelectSmemStaged, st, 0, a);
+  else
+    launch_k(select_positions_kernel<BLOCK, false>, dim3(rows), dim3(kSelCta), kSelectSmemBase, st, 0, a);
+  return cudaGetLastError();
+}
+
+template <int BLOCK>
 static cudaError_t reindex_impl(IdxArgs &a, cudaStream_t st) {
   select_smem_optin<BLOCK>();
   launch_positions<BLOCK>(a, st);
@@ -1588,6 +1643,7 @@ static IdxArgs make_args(const csa2_cache &c, const uint16_t *q, const float *w,
   a.c = c; a.q = q; a.w = w; a.max_len = max_len; a.n_keep = n_keep; a.topk = topk; a.ws = ws;
   a.pool_out = nullptr; a.pool_in = nullptr; a.topk_out = nullptr;
   a.sigma_out = ws.sigma; a.sigma_stride = ws.sigma_stride;
+  a.row_seq = nullptr; a.row_pos = nullptr;
   a.d_err = d_err; a.use_pool = 0;
   return a;
 }
@@ -1624,6 +1680,22 @@ cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const 
   a.topk_out = topk_idx;
   a.use_pool = 1;
   CSA2_DISPATCH_BLOCK(block, reindex_impl<BL>(a, st));
+}
+
+// Verify rows: the Reindex stage per query row (session q_seq[r], causal limit q_pos[r]).
+cudaError_t launch_verify_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
+                                 const int64_t *q_pos, int64_t T, const int32_t *pool, int block, int n_keep, int topk,
+                                 int64_t max_len, int32_t *topk_idx, const IndexerWs &ws, int32_t *d_err,
+                                 cudaStream_t st) {
+  cudaError_t e = zero_ws(ws, st);
+  if (e != cudaSuccess) return e;
+  IdxArgs a = make_args(c, q, w, max_len, n_keep, topk, ws, d_err);
+  a.pool_in = pool;
+  a.topk_out = topk_idx;
+  a.use_pool = 1;
+  a.row_seq = q_seq;
+  a.row_pos = q_pos;
+  CSA2_DISPATCH_BLOCK(block, verify_impl<BL>(a, (int)T, st));
 }
 
 cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len,

@@ -8,6 +8,14 @@ pool with its own indexer queries, every Reuse layer passes the indices on,
 and every layer runs sparse attention over its indices plus its own
 128-token FP8 window.
 
+With ``drafts`` > 1 the step verifies speculative drafts (origotech.dev deep
+dive, section "아키텍처는 어떻게 KV 캐시를 줄이나", the DSpark item): the last
+``drafts`` positions of each session are appended together and each gets its
+own query row.  The Full layer keeps one pool per session, scored with the
+queries of the session's last row (whose causal context is the whole session);
+every row of every indexer layer then takes its top-k from that shared pool,
+limited to positions up to its own.
+
 All compute happens in libcsa2.so; this module allocates device memory with
 torch, fills caches from seeded synthetic inputs and sequences the calls
 (optionally captured into one CUDA graph).
@@ -22,8 +30,9 @@ import torch
 import synth
 from synth.workloads import FULL, REINDEX, REUSE, DecodeWorkload
 
-from . import (Cache, SwaRing, OP_ATTN_DECODE, OP_FULL_SELECT, alloc_workspace, indexer_full_select,
-               indexer_reindex_select, kv_append_fp4, sparse_attn_decode, workspace_bytes)
+from . import (Cache, SwaRing, OP_ATTN_DECODE, OP_FULL_SELECT, OP_VERIFY_SELECT, alloc_workspace,
+               indexer_full_select, indexer_reindex_select, indexer_verify_select, kv_append_fp4, sparse_attn_decode,
+               workspace_bytes)
 
 
 def _to_dev(a: np.ndarray, dtype, device):
@@ -41,6 +50,9 @@ class DecodeRunner:
         self.wl = wl
         self.device = device
         B = wl.B
+        self.D = int(wl.drafts)
+        self.T = B * self.D
+        assert self.D >= 1 and wl.ring >= wl.window + self.D - 1, "ring must hold every draft row's window"
         L = wl.lengths.astype(np.int64)
         self.lengths = L
         self.max_len = int(L.max())
@@ -63,24 +75,26 @@ class DecodeRunner:
 
     # ------------------------------------------------------------------ inputs
     def _make_step_inputs(self):
-        wl, dev, B = self.wl, self.device, self.wl.B
+        wl, dev, B, D, T = self.wl, self.device, self.wl.B, self.D, self.T
         s = wl.seed
-        newpos = self.lengths - 1
-        rows_new = synth.row_id(np.arange(B), newpos)
+        # query row r = b * D + j is position L_b - D + j of sequence b
+        seq = np.repeat(np.arange(B), D)
+        newpos = np.repeat(self.lengths, D) - D + np.tile(np.arange(D), B)
+        rows_new = synth.row_id(seq, newpos)
         self.h_kv_new = synth.normals_bf16(s, synth.Stream.KV, 0, rows_new, 128, self.kv_outliers)
         self.h_ik_new = synth.normals_bf16(s, synth.Stream.IK, 0, rows_new, 64)
         self.h_swa_new = np.stack([synth.normals_bf16(s, synth.Stream.SWA, l, rows_new, 128, self.swa_outliers)
                                    for l in range(wl.n_layers)])
-        self.h_seq_id = np.arange(B, dtype=np.int32)
+        self.h_seq_id = seq.astype(np.int32)
         self.h_pos = newpos.astype(np.int64)
         self.h_q = np.stack([synth.normals_bf16(s, synth.Stream.Q, l,
-                                                synth.row_id(np.repeat(np.arange(B), wl.H), np.tile(np.arange(wl.H), B)),
-                                                128).reshape(B, wl.H, 128) for l in range(wl.n_layers)])
+                                                synth.row_id(np.repeat(np.arange(T), wl.H), np.tile(np.arange(wl.H), T)),
+                                                128).reshape(T, wl.H, 128) for l in range(wl.n_layers)])
         self.idx_layers = [l for l, m in enumerate(wl.schedule) if m in (FULL, REINDEX)]
         self.h_qidx = {l: synth.normals_bf16(s, synth.Stream.QIDX, l,
-                                             synth.row_id(np.repeat(np.arange(B), 8), np.tile(np.arange(8), B)),
-                                             64).reshape(B, 8, 64) for l in self.idx_layers}
-        self.h_w = {l: np.stack([synth.head_weights(s, l, b) for b in range(B)]) for l in self.idx_layers}
+                                             synth.row_id(np.repeat(np.arange(T), 8), np.tile(np.arange(8), T)),
+                                             64).reshape(T, 8, 64) for l in self.idx_layers}
+        self.h_w = {l: np.stack([synth.head_weights(s, l, r) for r in range(T)]) for l in self.idx_layers}
         # device copies
         self.kv_new = _bf16_dev(self.h_kv_new, dev)
         self.ik_new = _bf16_dev(self.h_ik_new, dev)
@@ -90,16 +104,24 @@ class DecodeRunner:
         self.q = _bf16_dev(self.h_q, dev)
         self.qidx = {l: _bf16_dev(v, dev) for l, v in self.h_qidx.items()}
         self.w = {l: _to_dev(v, torch.float32, dev) for l, v in self.h_w.items()}
+        # the Full layer's pool is scored with each session's last row: a step input of its own
+        self.full_layers = [l for l in self.idx_layers if wl.schedule[l] == FULL]
+        self.qidx_last = {l: self.qidx[l][D - 1::D].contiguous() if D > 1 else self.qidx[l] for l in self.full_layers}
+        self.w_last = {l: self.w[l][D - 1::D].contiguous() if D > 1 else self.w[l] for l in self.full_layers}
 
     def _make_outputs(self):
-        wl, dev, B = self.wl, self.device, self.wl.B
+        wl, dev, B, T = self.wl, self.device, self.wl.B, self.T
         self.pool = torch.full((B, wl.n_keep), -1, dtype=torch.int32, device=dev)
-        self.topk = {l: torch.full((B, wl.topk), -1, dtype=torch.int32, device=dev) for l in self.idx_layers}
-        self.out = torch.zeros((wl.n_layers, B, wl.H, 128), dtype=torch.float32, device=dev)
-        self.lse = torch.zeros((wl.n_layers, B, wl.H), dtype=torch.float32, device=dev)
+        self.topk = {l: torch.full((T, wl.topk), -1, dtype=torch.int32, device=dev) for l in self.idx_layers}
+        self.topk_full = {l: (torch.full((B, wl.topk), -1, dtype=torch.int32, device=dev) if self.D > 1
+                              else self.topk[l]) for l in self.full_layers}
+        self.out = torch.zeros((wl.n_layers, T, wl.H, 128), dtype=torch.float32, device=dev)
+        self.lse = torch.zeros((wl.n_layers, T, wl.H), dtype=torch.float32, device=dev)
         self.ws_idx = alloc_workspace(workspace_bytes(OP_FULL_SELECT, B, self.max_len, wl.block, wl.n_keep, wl.topk),
                                       dev)
-        self.ws_attn = alloc_workspace(workspace_bytes(OP_ATTN_DECODE, T=B, H=wl.H, topk=wl.topk, window=wl.window),
+        self.ws_ver = (alloc_workspace(workspace_bytes(OP_VERIFY_SELECT, block=wl.block, n_keep_blocks=wl.n_keep,
+                                                       topk=wl.topk, T=T), dev) if self.D > 1 else None)
+        self.ws_attn = alloc_workspace(workspace_bytes(OP_ATTN_DECODE, T=T, H=wl.H, topk=wl.topk, window=wl.window),
                                        dev)
         self.tau = 1.0 / math.sqrt(128.0)
 
@@ -110,10 +132,10 @@ class DecodeRunner:
 
     # ------------------------------------------------------------------ cache build
     def build_cache(self, chunk: int = 1 << 18):
-        """Append positions 0..L-2 of every sequence (the step appends L-1) and the window rows."""
+        """Append positions 0..L-D-1 of every sequence (the step appends the last D) and the window rows."""
         wl, dev, s = self.wl, self.device, self.wl.seed
         for b in range(wl.B):
-            n_old = int(self.lengths[b]) - 1
+            n_old = int(self.lengths[b]) - self.D
             for lo in range(0, n_old, chunk):
                 hi = min(n_old, lo + chunk)
                 pos = np.arange(lo, hi, dtype=np.int64)
@@ -138,14 +160,18 @@ class DecodeRunner:
 
     # ------------------------------------------------------------------ the step
     def step(self, prof=None):
-        """One decode step through every layer of the schedule."""
+        """One decode (or draft-verification) step through every layer of the schedule."""
         wl = self.wl
         kv_append_fp4(self.cache, self.swa, self.kv_new, self.ik_new, self.swa_new, self.rope_cos, self.rope_sin,
                       self.seq_id, self.pos, self.d_err)
         for l, mode in enumerate(wl.schedule):
             if mode == FULL:
-                indexer_full_select(self.cache, self.qidx[l], self.w[l], wl.block, wl.n_keep, wl.topk, self.max_len,
-                                    self.pool, self.topk[l], self.ws_idx, self.d_err, prof=prof)
+                indexer_full_select(self.cache, self.qidx_last[l], self.w_last[l], wl.block, wl.n_keep, wl.topk,
+                                    self.max_len, self.pool, self.topk_full[l], self.ws_idx, self.d_err, prof=prof)
+            if self.D > 1 and mode in (FULL, REINDEX):
+                indexer_verify_select(self.cache, self.qidx[l], self.w[l], self.seq_id, self.pos, self.pool,
+                                      wl.block, wl.n_keep, wl.topk, self.max_len, self.topk[l], self.ws_ver,
+                                      self.d_err)
             elif mode == REINDEX:
                 indexer_reindex_select(self.cache, self.qidx[l], self.w[l], self.pool, wl.block, wl.n_keep, wl.topk,
                                        self.max_len, self.topk[l], self.ws_idx, self.d_err)

@@ -39,6 +39,7 @@ class DecodeWorkload:
     window: int = 128
     ring: int = 128                # SWA ring slots per sequence and layer
     seed: int = 0
+    drafts: int = 1                # query rows per sequence: the last `drafts` positions, all appended this step
 
     @property
     def B(self) -> int:
@@ -59,6 +60,16 @@ class ChunkedWorkload:
     window: int = 128
     ring: int = 8192               # SWA ring large enough to hold every query's window
     seed: int = 0
+
+
+def verify_workload():
+    """Speculative verification: 32 sessions of 65,536 tokens whose last 5 positions are drafted
+    tokens, each verified by its own query row through the 20-layer schedule (origotech.dev deep
+    dive, section "아키텍처는 어떻게 KV 캐시를 줄이나": the DSpark drafter proposes 5 positions at
+    once).  The ring holds window + 4 positions so that the earliest draft row still sees its
+    whole window."""
+    return DecodeWorkload("verify_b32_ctx65536_d5_20layer", np.full(32, 65536, dtype=np.int64),
+                          schedule=decoder_schedule(20), drafts=5, ring=256)
 
 
 def config(i: int):

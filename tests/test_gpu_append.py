@@ -148,3 +148,65 @@ def test_append_rejects_bad_arguments_before_launch():
         csa2.kv_append_fp4(cache, None, kv.view(-1)[1:], None, None, dev(cos), dev(sin), dev(np.zeros(1, np.int32)),
                            dev(np.zeros(1, np.int64)), d_err)   # misaligned bf16 rows
     assert e.value.status == csa2.ERR_INVALID_ARG
+
+
+def test_swa_refill_rebuilds_rings_bit_exact():
+    # replay of the last window of each sequence into fresh rings; ring slots that no
+    # replayed token maps to keep their old contents
+    B, n_layers, ring = 3, 4, 128
+    lengths = [37, 300, 1000]
+    swa = [csa2.SwaRing(B, ring) for _ in range(n_layers)]
+    for r in swa:
+        r.codes.fill_(0x5A)
+        r.scale.fill_(7.0)
+    seq = np.concatenate([np.full(min(L, ring), b, np.int32) for b, L in enumerate(lengths)])
+    pos = np.concatenate([np.arange(max(0, L - ring), L, dtype=np.int64) for L in lengths])
+    rows = synth.row_id(seq, pos)
+    soc = synth.outlier_channels(0, synth.Stream.SWA_OUTLIER)
+    sw = np.stack([synth.normals_bf16(0, synth.Stream.SWA, l, rows, 128, soc) for l in range(n_layers)])
+    cos, sin = synth.rope_table(1100)
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.swa_refill_fp8(swa, B, dev_bf16(sw), dev(cos), dev(sin), dev(seq), dev(pos), d_err)
+    torch.cuda.synchronize()
+    assert int(d_err.item()) == 0
+    for l in range(n_layers):
+        sc, ss = swa_rows(sw[l], cos[pos], sin[pos])
+        codes, scale = host(swa[l].codes), host(swa[l].scale)
+        assert np.array_equal(codes[seq, pos % ring], sc)
+        assert np.array_equal(scale[seq, pos % ring].view(np.uint32), ss.view(np.uint32))
+        untouched = np.ones((B, ring), bool)
+        untouched[seq, pos % ring] = False
+        assert np.all(codes[untouched] == 0x5A) and np.all(scale[untouched] == 7.0)
+
+
+def test_swa_refill_matches_the_append_window_bytes_and_flags_bad_tokens():
+    B, n_layers, ring = 2, 2, 128
+    cache, swa_a, _ = _small_cache(B, [200, 64], n_layers, ring)
+    swa_r = [csa2.SwaRing(B, ring) for _ in range(n_layers)]
+    seq = np.array([0, 1, 0, 1, 5], np.int32)          # the last token has a bad sequence id
+    pos = np.array([199, 63, 150, 10, 3], np.int64)
+    rows = synth.row_id(seq, pos)
+    kv = synth.normals_bf16(1, synth.Stream.KV, 0, rows, 128)
+    sw = np.stack([synth.normals_bf16(1, synth.Stream.SWA, l, rows, 128) for l in range(n_layers)])
+    cos, sin = synth.rope_table(256)
+    e1 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    e2 = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.kv_append_fp4(cache, swa_a, dev_bf16(kv), None, dev_bf16(sw), dev(cos), dev(sin), dev(seq), dev(pos), e1)
+    csa2.swa_refill_fp8(swa_r, B, dev_bf16(sw), dev(cos), dev(sin), dev(seq), dev(pos), e2)
+    torch.cuda.synchronize()
+    assert int(e1.item()) == csa2.DEVERR_SEQ and int(e2.item()) == csa2.DEVERR_SEQ
+    for l in range(n_layers):
+        assert torch.equal(swa_a[l].codes, swa_r[l].codes) and torch.equal(swa_a[l].scale, swa_r[l].scale)
+
+
+def test_swa_refill_rejects_bad_arguments_before_launch():
+    swa = [csa2.SwaRing(1, 128)]
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    x = torch.zeros((1, 1, 128), dtype=torch.bfloat16, device="cuda")
+    cos = torch.zeros((4, 32), dtype=torch.float32, device="cuda")
+    one = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p = torch.zeros(1, dtype=torch.int64, device="cuda")
+    with pytest.raises(csa2.Csa2Error):
+        csa2.swa_refill_fp8([], 1, x, cos, cos, one, p, d_err)                    # no layers
+    with pytest.raises(csa2.Csa2Error):
+        csa2.swa_refill_fp8(swa, 0, x, cos, cos, one, p, d_err)                   # B < 1

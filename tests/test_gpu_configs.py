@@ -15,7 +15,7 @@ import torch
 import synth
 from oracle import pipeline
 from oracle import indexer as ix
-from synth.workloads import config, FULL, REINDEX
+from synth.workloads import config, verify_workload, FULL, REINDEX
 from tests.gpu_util import ATTN_TOL, attn_rel_err, check_index_set, csa2
 
 pytestmark = pytest.mark.gpu
@@ -48,7 +48,7 @@ def _check_sequence(r, wl, b, layers=None):
 
 def _runner(cfg):
     from sparse_attention_fp4_02_b300.runner import DecodeRunner
-    wl = config(cfg)
+    wl = config(cfg) if isinstance(cfg, int) else cfg
     r = DecodeRunner(wl)
     r.build_cache()
     r.step()
@@ -99,3 +99,32 @@ def test_config3_chunked_queries_h64_cache262144():
     # every row's output is a convex combination: finite, and lse finite
     assert np.all(np.isfinite(out)) and np.all(np.isfinite(lse))
     print("max rel err", e)
+
+
+def test_verify_b32_ctx65536_five_drafts_twenty_layers():
+    """Draft verification: 5 query rows per session, one shared pool, causal per-row top-k."""
+    wl = verify_workload()
+    wl, r = _runner(wl)
+    D, L = wl.drafts, int(wl.lengths[0])
+    for b in (0, 19, 31):
+        ref = pipeline.decode_step(wl, b, layers=[0, 1, 4, 7, 19])
+        _, _, ic, isc = ref["cache"]
+        bs = ix.block_scores(ref["sigma"][0], wl.block)
+        swaps = check_index_set(r.pool[b].cpu().numpy(), ref["pool"], lambda j: bs[j], f"pool b={b}")
+        for l, otop in ref["topk"].items():
+            for j in range(D):
+                g = r.topk[l][b * D + j].cpu().numpy()
+                qi = pipeline.layer_inputs(wl, b, l, j)
+                p = L - D + j
+                score = ix.scores(qi[1], qi[2], ic[:p + 1], isc[:p + 1])
+                swaps += check_index_set(g, otop[j], lambda t: score[t], f"topk layer {l} b={b} row {j}")
+                assert np.all(g[g >= 0] <= p)
+        worst = 0.0
+        if swaps == 0:
+            for l, o in ref["out"].items():
+                rows = slice(b * D, b * D + D)
+                e = attn_rel_err(r.out[l, rows].cpu().numpy(), o)
+                le = float(np.max(np.abs(r.lse[l, rows].cpu().numpy() - ref["lse"][l])))
+                assert e <= ATTN_TOL and le <= 1e-4, (l, e, le)
+                worst = max(worst, e)
+        print(b, "swaps", swaps, "max rel err", worst)

@@ -114,6 +114,34 @@ def test_reindex_picks_only_pool_positions_and_reuse_is_identity():
     assert chosen.min() >= full_sig[others].max()
 
 
+def test_verify_rows_rank_the_pool_up_to_their_own_position():
+    rng = np.random.default_rng(13)
+    L = 4000
+    codes, scale = _tiny_keys(rng, L)
+    q, w = _tiny_q(rng)
+    pool, _, _ = indexer.full_select(q, w, codes, scale, block=8, n_keep=120, topk=50)
+    allowed_all = indexer.pool_positions(pool, L, 8)
+    q2, w2 = _tiny_q(rng)
+    # the last position of the context: the plain Reindex rule
+    v, _, _ = indexer.verify_select(q2, w2, codes, scale, pool, L - 1, 8, 50)
+    r, _, _ = indexer.reindex_select(q2, w2, codes, scale, pool, 8, 50)
+    assert np.array_equal(v, r)
+    full_sig = indexer.scores(q2, w2, codes, scale)
+    for p in (int(allowed_all[40]), int(allowed_all[300]) - 1, 2500):
+        v, _, _ = indexer.verify_select(q2, w2, codes, scale, pool, p, 8, 50)
+        allowed = allowed_all[allowed_all <= p]
+        got = v[v >= 0]
+        # brute force: the min(50, |allowed|) best allowed positions, nothing after p
+        assert got.shape[0] == min(50, allowed.shape[0]) and np.all(got <= p)
+        assert set(got.tolist()) <= set(allowed.tolist()) and np.all(np.diff(got) > 0)
+        rest = np.array(sorted(set(allowed.tolist()) - set(got.tolist())), np.int64)
+        if rest.size:
+            assert full_sig[got].min() >= full_sig[rest].max()
+    # a position before the first pool block selects nothing
+    v, _, _ = indexer.verify_select(q2, w2, codes, scale, pool, int(allowed_all[0]) - 1, 8, 50)
+    assert np.all(v == -1)
+
+
 def test_pool_is_2048_blocks_of_8_at_decoder_sizes():
     rng = np.random.default_rng(11)
     L = 20000
@@ -156,3 +184,25 @@ def test_planted_indexer_mistakes_are_caught(planted, monkeypatch):
     _, bt, _ = bruteforce.select(bf16_to_f32(q).astype(np.float64).tolist(), w.astype(np.float64).tolist(),
                                  codes.tolist(), scale.astype(np.float64).tolist(), 8, 4, 6)
     assert list(top[top >= 0]) != bt
+
+
+def test_verify_step_last_row_of_the_full_layer_equals_its_full_top_k():
+    """Containment: the last draft row sees the whole context, so its top-k from the shared pool
+    equals the Full top-k over every position; earlier rows stay inside their own prefix."""
+    from oracle import pipeline
+    from synth.workloads import DecodeWorkload, FULL, REINDEX, REUSE
+    wl = DecodeWorkload("tiny_verify", np.array([2000, 700], np.int64), schedule=[FULL, REUSE, REINDEX],
+                        n_keep=40, topk=24, ring=256, drafts=4)
+    for b in range(2):
+        st = pipeline.prepare(wl, b, layers=[0, 2])
+        res = pipeline.step(wl, b, st, with_attention=False)
+        _, _, ic, isc = st["cache"]
+        _, qi, w = st["inputs"][0]
+        _, top, _ = indexer.full_select(qi, w, ic, isc, wl.block, wl.n_keep, wl.topk)
+        assert np.array_equal(res["topk"][0][-1], top)
+        L = int(wl.lengths[b])
+        for l in (0, 2):
+            assert res["topk"][l].shape == (4, wl.topk)
+            for j in range(4):
+                got = res["topk"][l][j]
+                assert np.all(got[got >= 0] <= L - 4 + j)
