@@ -1255,22 +1255,45 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
   const int32_t *m1 = m1c <= kListCap ? s_m1 : g_m1;
   const int32_t *m2 = m2c <= kListCap ? s_m2 : g_m2;
 
-  // ---- pool
-  if (sel_pool) {
-    const bool big = m1c > kListCap;
-    int32_t *band = big ? g_m1 + 2 * a.ws.unc_x : s_band;
-    float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : s_ex;
-    auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
-      QFrag f;
-      QExact q;
-      load_qfrag(qb, wb, lane, f);
-      load_qexact(qb, wb, lane, q);
-      exact_block_maxima<BLOCK>(a, e, f, q, E, bd, xv, u, id, s_lut);
-    };
-    resolve_list(m1, m1c, k1, cert1, w1_lo, w1_hi, E, val, id, exact_band, pick_pool, band, ex, s_hist, s_cnt,
-                 s_scan, s_out);
+  // ---- pool.  With two CTAs per sequence (gridDim.y == 2) CTA 0 selects and writes the pool
+  // while CTA 1 selects the top-k positions; CTA 1 needs the pool itself only when the
+  // candidate blocks outnumber it.
+  const bool split = gridDim.y > 1;
+  auto run_pool = [&]() {
+    if (sel_pool) {
+      const bool big = m1c > kListCap;
+      int32_t *band = big ? g_m1 + 2 * a.ws.unc_x : s_band;
+      float2 *ex = big ? a.ws.unc_val + (int64_t)b * a.ws.unc_x : s_ex;
+      auto exact_band = [&](const int32_t *bd, float2 *xv, int u) {
+        QFrag f;
+        QExact q;
+        load_qfrag(qb, wb, lane, f);
+        load_qexact(qb, wb, lane, q);
+        exact_block_maxima<BLOCK>(a, e, f, q, E, bd, xv, u, id, s_lut);
+      };
+      resolve_list(m1, m1c, k1, cert1, w1_lo, w1_hi, E, val, id, exact_band, pick_pool, band, ex, s_hist, s_cnt,
+                   s_scan, s_out);
+    }
+    __syncthreads();
+    if (sel_pool && !use_bits) {
+      cta_sort_asc(s_sort, k1);                                   // k1 <= n_keep <= 4096 ids
+      __syncthreads();
+    }
+  };
+  bool pool_done = false;
+  if (!split || blockIdx.y == 0) {
+    run_pool();
+    pool_done = true;
+    if (!sel_pool) {
+      for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < nb ? i : -1;
+    } else if (use_bits) {
+      emit_bits_ascending(s_pool_bits, nwords, [](int i) { return (int32_t)i; }, pool, n_keep, s_scan);
+    } else {
+      for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < k1 ? s_sort[i] : -1;
+    }
+    __syncthreads();
+    if (split) return;
   }
-  __syncthreads();
   // ---- position-candidate blocks: the topk-th largest approximate maximum, lower cut
   if (sel_pcb) {
     const uint32_t kth = list_kth(m2, m2c, [&](int i) { return __float_as_uint(val(i)); }, k2 - cert2,
@@ -1284,16 +1307,6 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
   }
   __syncthreads();
 
-  // ---- emit, ascending
-  if (!sel_pool) {
-    for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < nb ? i : -1;
-  } else if (use_bits) {
-    emit_bits_ascending(s_pool_bits, nwords, [](int i) { return (int32_t)i; }, pool, n_keep, s_scan);
-  } else {
-    cta_sort_asc(s_sort, k1);                                     // k1 <= n_keep <= 4096 ids
-    for (int i = tid; i < n_keep; i += blockDim.x) pool[i] = i < k1 ? s_sort[i] : -1;
-  }
-  __syncthreads();
   // ---- the candidate blocks, ascending, into shared memory
   int32_t *s_list = s_m1;                                          // m1 + m2: 2 kListCap >= kMaxSel ids
   int count;
@@ -1310,6 +1323,7 @@ __global__ void __launch_bounds__(kSelCta, 1) finalize_blocks_kernel(const __gri
     const int n_pcb = s_cnt[kCntPcb];
     if (!use_bits || n_pcb > n_keep) {
       // the pool contains every top-k position's block
+      if (!pool_done) run_pool();
       if (!sel_pool) for (int i = tid; i < nb; i += blockDim.x) s_list[i] = i;
       else if (use_bits) emit_bits_ascending(s_pool_bits, nwords, [](int i) { return (int32_t)i; }, s_list, n_keep, s_scan);
       else for (int i = tid; i < k1; i += blockDim.x) s_list[i] = s_sort[i];
@@ -1571,12 +1585,23 @@ static void select_smem_optin() {
   }
 }
 
-static int positions_grid(int B) { return std::max(1, std::min(32, (int)((int64_t)num_sms() * 2 / std::max(B, 1)))); }
+// CTAs per row of the position scoring: enough resident warps on every SM, at most 32 per row.
+template <int BLOCK>
+static int positions_grid(int rows) {
+  static int resident = 0;
+  if (resident == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_positions_kernel<BLOCK>, 256, 0) != cudaSuccess || n < 1)
+      n = 2;
+    resident = std::min(n, 4);
+  }
+  return std::max(1, std::min(32, (int)((int64_t)num_sms() * resident / std::max(rows, 1))));
+}
 
 template <int BLOCK>
 static void launch_positions(IdxArgs &a, cudaStream_t st) {
   const int B = a.c.B;
-  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid(B), B), dim3(256), 0, st, 0, a);
+  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid<BLOCK>(B), B), dim3(256), 0, st, 0, a);
   if ((int64_t)a.n_keep * BLOCK <= kStageItems)
     launch_k(select_positions_kernel<BLOCK, true>, dim3(B), dim3(kSelCta), kSelectSmemStaged, st, 0, a);
   else
@@ -1595,12 +1620,14 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
   launch_scan<BLOCK, true>(a, max_len, st);
   if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
   const int64_t nbm = a.ws.nbm;
+  // pool and top-k positions in separate CTAs while both fit in one wave (one CTA per SM)
+  const dim3 fin((unsigned)B, 2 * B <= num_sms() ? 2u : 1u);
   if (nbm <= kDirectBlocks) {
-    launch_k(finalize_blocks_kernel<BLOCK, true>, dim3(B), dim3(kSelCta), kFinalizeSmemDirect, st, 0, a);
+    launch_k(finalize_blocks_kernel<BLOCK, true>, fin, dim3(kSelCta), kFinalizeSmemDirect, st, 0, a);
   } else {
     dim3 cg((unsigned)((nbm + kCollectPer - 1) / kCollectPer), (unsigned)B);
     launch_k(collect_kernel<BLOCK>, cg, dim3(256), 0, st, 0, a);
-    launch_k(finalize_blocks_kernel<BLOCK, false>, dim3(B), dim3(kSelCta), kFinalizeSmemCand, st, 0, a);
+    launch_k(finalize_blocks_kernel<BLOCK, false>, fin, dim3(kSelCta), kFinalizeSmemCand, st, 0, a);
   }
   return cudaGetLastError();
 }
@@ -1608,7 +1635,7 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
 template <int BLOCK>
 static cudaError_t verify_impl(IdxArgs &a, int rows, cudaStream_t st) {
   select_smem_optin<BLOCK>();
-  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid(rows), rows), dim3(256), 0, st, 0, a);
+  launch_k(score_positions_kernel<BLOCK>, dim3(positions_grid<BLOCK>(rows), rows), dim3(256), 0, st, 0, a);
   if ((int64_t)a.n_keep * BLOCK <= kStageItems)
     launch_k(select_positions_kernel<BLOCK, true>, dim3(rows), dim3(kSelCta), kSelectSmemStaged, st, 0, a);
   else
