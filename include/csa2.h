@@ -120,7 +120,8 @@ enum csa2_op {
   CSA2_OP_FULL_SELECT = 1,
   CSA2_OP_REINDEX_SELECT = 2,
   CSA2_OP_ATTN_DECODE = 3,
-  CSA2_OP_VERIFY_SELECT = 4
+  CSA2_OP_VERIFY_SELECT = 4,
+  CSA2_OP_CHUNKED_SELECT = 5
 };
 
 /* Human-readable name of a status code (static string). */
@@ -131,6 +132,7 @@ const char *csa2_status_string(int status);
  *   FULL_SELECT / REINDEX_SELECT: B, max_len, block, n_keep_blocks, topk used.
  *   ATTN_DECODE: T (query rows), H (heads), topk, window used.
  *   VERIFY_SELECT: T (query rows), block, n_keep_blocks, topk used.
+ *   CHUNKED_SELECT: T (query rows), max_len, block, n_keep_blocks, topk used.
  * Returns CSA2_ERR_INVALID_ARG for out-of-range sizes.  Workspace must be
  * 256-byte aligned; its contents need not be initialised and are clobbered.
  */
@@ -250,6 +252,28 @@ int indexer_reindex_select_static(const csa2_cache *cache, const uint16_t *q_idx
                                   const int32_t *pool_blocks, int32_t block, int32_t n_keep_blocks,
                                   int32_t topk, int64_t max_len, int32_t *topk_idx, int32_t *d_err,
                                   csa2_stream_t stream);
+
+/*
+ * indexer_chunked_select - the Full layer's selection for many query rows at once, each
+ * over its session's positions up to its own (a chunk of prefill queries).
+ * (origotech.dev deep dive, subsection "Compressed Sparse Attention 2(CSA2)": a Full
+ * layer scores every cached position with its own indexer queries and keeps 2,048 blocks
+ * of 8 plus the top-512 positions; a query sees the positions up to its own)
+ *   q_idx          bf16 [T][8][64], w float [T][8]: each row's indexer queries and weights
+ *   q_seq, q_pos   int32 [T], int64 [T]: session and position of each row
+ *   T              rows, 0..2^24
+ *   max_len        >= q_pos[r] + 1 for every row (bounds the workspace)
+ *   pool_blocks    int32 [T][n_keep_blocks] out, topk_idx int32 [T][topk] out: for row r,
+ *                  exactly what indexer_full_select returns for a session made of the
+ *                  first q_pos[r] + 1 positions of session q_seq[r]
+ *   ws/ws_bytes    csa2_workspace_bytes(CSA2_OP_CHUNKED_SELECT, ...)
+ * Rows are processed in groups of CSA2_MAX_B.  A row with a bad q_seq or q_pos selects
+ * nothing (all -1) and sets CSA2_DEVERR_SEQ / _POS.
+ */
+int indexer_chunked_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                           const int64_t *q_pos, int64_t T, int32_t block, int32_t n_keep_blocks, int32_t topk,
+                           int64_t max_len, int32_t *pool_blocks, int32_t *topk_idx, void *ws, size_t ws_bytes,
+                           int32_t *d_err, csa2_stream_t stream);
 
 /*
  * indexer_verify_select - the Reindex selection for several query rows per session,

@@ -97,6 +97,13 @@ def reindex_select(q_bf16, w, ik_codes, ik_scale, pool, block=8, topk=512):
     return pad(top_k_ids(sigma, pos, topk), topk), sigma, pos
 
 
+def chunked_select(q_bf16, w, ik_codes, ik_scale, p: int, block=8, n_keep=2048, topk=512):
+    """One row of a chunk of prefill queries, at position p: the Full selection (pool +
+    top-k) over positions 0..p only, a query seeing nothing after itself (origotech.dev deep
+    dive, subsection "Compressed Sparse Attention 2(CSA2)")."""
+    return full_select(q_bf16, w, ik_codes[:p + 1], ik_scale[:p + 1], block, n_keep, topk)
+
+
 def verify_select(q_bf16, w, ik_codes, ik_scale, pool, p: int, block=8, topk=512):
     """One verify row at position p: top-k over the session's pool positions p' <= p.
 

@@ -7,7 +7,7 @@ library has not been built, importing this package raises: there is no CPU
 fallback.
 
 Entry points (same names as the C ABI): ``kv_append_fp4``, ``swa_refill_fp8``,
-``indexer_full_select``, ``indexer_reindex_select``, ``indexer_verify_select``, ``sparse_attn_decode``,
+``indexer_full_select``, ``indexer_reindex_select``, ``indexer_verify_select``, ``indexer_chunked_select``, ``sparse_attn_decode``,
 plus ``workspace_bytes`` and the ``Cache`` / ``SwaRing`` containers that own
 the device tensors of the layouts the header documents.
 """
@@ -28,7 +28,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 OK, ERR_INVALID_ARG, ERR_WORKSPACE, ERR_UNSUPPORTED, ERR_CUDA, ERR_DEVICE_TIMEOUT = range(6)
 DEVERR_SEQ, DEVERR_POS, DEVERR_LEN, DEVERR_INDEX, DEVERR_POOL, DEVERR_TIMEOUT = 1, 2, 4, 8, 16, 32
-OP_FULL_SELECT, OP_REINDEX_SELECT, OP_ATTN_DECODE, OP_VERIFY_SELECT = 1, 2, 3, 4
+OP_FULL_SELECT, OP_REINDEX_SELECT, OP_ATTN_DECODE, OP_VERIFY_SELECT, OP_CHUNKED_SELECT = 1, 2, 3, 4, 5
 D, D_IDX, H_IDX = 128, 64, 8
 MAX_SWA_LAYERS = 32
 
@@ -67,6 +67,8 @@ _refill = _sig("swa_refill_fp8", [_P, _I32, _I32, _P, _P, _P, _I64, _P, _P, _I64
 _full = _sig("indexer_full_select", [_P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P, _SZ, _P, _P, _P])
 _reindex = _sig("indexer_reindex_select", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _SZ, _P, _P])
 _reindex_static = _sig("indexer_reindex_select_static", [_P, _P, _P, _P, _I32, _I32, _I32, _I64, _P, _P, _P])
+_chunked = _sig("indexer_chunked_select", [_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _P, _P, _P, _SZ, _P,
+                                           _P])
 _verify = _sig("indexer_verify_select", [_P, _P, _P, _P, _P, _I64, _P, _I32, _I32, _I32, _I64, _P, _P, _SZ, _P,
                                          _P])
 _attn = _sig("sparse_attn_decode", [_P, _P, _P, _I32, _I64, _P, _P, _P, _I32, _I32, _F32, _P, _P, _P, _SZ,
@@ -76,7 +78,7 @@ _t_fp8 = _sig("csa2_test_quantize_fp8", [_P, _I64, _I32, _P, _P, _P])
 _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _P, _P])
 
 EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "swa_refill_fp8", "indexer_full_select",
-            "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
+            "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select", "indexer_chunked_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
             "csa2_test_quantize_fp8", "csa2_test_index_scores")
 
 
@@ -188,6 +190,14 @@ def indexer_reindex_select_static(cache: Cache, q_idx, w, pool_blocks, block, n_
     _check(_reindex_static(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(pool_blocks), block,
                            n_keep_blocks, topk, int(max_len), _ptr(topk_idx), _ptr(d_err), _stream(stream)),
            "indexer_reindex_select_static")
+
+
+def indexer_chunked_select(cache: Cache, q_idx, w, q_seq, q_pos, block, n_keep_blocks, topk, max_len, pool_blocks,
+                           topk_idx, ws, d_err, stream=None):
+    """Per query row: the Full selection over its session's positions up to its own."""
+    _check(_chunked(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(q_seq), _ptr(q_pos), int(q_seq.shape[0]),
+                    block, n_keep_blocks, topk, int(max_len), _ptr(pool_blocks), _ptr(topk_idx), _ptr(ws), ws.numel(),
+                    _ptr(d_err), _stream(stream)), "indexer_chunked_select")
 
 
 def indexer_verify_select(cache: Cache, q_idx, w, q_seq, q_pos, pool_blocks, block, n_keep_blocks, topk, max_len,

@@ -79,6 +79,11 @@ int csa2_workspace_bytes(int op, int32_t B, int64_t max_len, int32_t block, int3
       if (T < 0 || T > 65535 || !select_sizes_ok(1, 0, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
       *bytes = indexer_ws_bytes((int32_t)(T > 0 ? T : 1), 0, block, n_keep_blocks);
       return CSA2_OK;
+    case CSA2_OP_CHUNKED_SELECT:
+      if (T < 0 || T > (1 << 24) || !select_sizes_ok(1, max_len, block, n_keep_blocks, topk))
+        return CSA2_ERR_INVALID_ARG;
+      *bytes = chunked_ws_bytes(T, max_len, block, n_keep_blocks);
+      return CSA2_OK;
     case CSA2_OP_ATTN_DECODE:
       if (!attn_sizes_ok(T, H, topk, window)) return CSA2_ERR_INVALID_ARG;
       *bytes = attn_ws_bytes(T, H, topk, window);
@@ -166,6 +171,23 @@ int indexer_reindex_select(const csa2_cache *cache, const uint16_t *q_idx, const
   IndexerWs iw = indexer_ws_carve(ws, cache->B, max_len, block, n_keep_blocks);
   return cuda_status(launch_reindex_select(*cache, q_idx, w, pool_blocks, block, n_keep_blocks, topk, max_len,
                                            topk_idx, iw, d_err, (cudaStream_t)stream));
+}
+
+int indexer_chunked_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                           const int64_t *q_pos, int64_t T, int32_t block, int32_t n_keep_blocks, int32_t topk,
+                           int64_t max_len, int32_t *pool_blocks, int32_t *topk_idx, void *ws, size_t ws_bytes,
+                           int32_t *d_err, csa2_stream_t stream) {
+  if (!cache_ok(cache) || !d_err || T < 0 || T > (1 << 24)) return CSA2_ERR_INVALID_ARG;
+  if (!select_sizes_ok(1, max_len, block, n_keep_blocks, topk)) return CSA2_ERR_INVALID_ARG;
+  if (T == 0) return CSA2_OK;
+  if (!q_idx || !aligned(q_idx, 16) || !w || !aligned(w, 4) || !q_seq || !q_pos || !pool_blocks || !topk_idx)
+    return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < chunked_ws_bytes(T, max_len, block, n_keep_blocks))
+    return CSA2_ERR_WORKSPACE;
+  int st = device_ok();
+  if (st != CSA2_OK) return st;
+  return cuda_status(launch_chunked_select(*cache, q_idx, w, q_seq, q_pos, T, block, n_keep_blocks, topk, max_len,
+                                           pool_blocks, topk_idx, ws, d_err, (cudaStream_t)stream));
 }
 
 int indexer_verify_select(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,

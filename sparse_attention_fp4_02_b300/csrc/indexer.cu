@@ -1725,6 +1725,54 @@ cudaError_t launch_verify_select(const csa2_cache &c, const uint16_t *q, const f
   CSA2_DISPATCH_BLOCK(block, verify_impl<BL>(a, (int)T, st));
 }
 
+// Chunked queries: every query row gets the Full selection over its session's positions up
+// to its own.  A small kernel turns (session, position) into a per-row view of the cache
+// (the session's base, length position + 1); groups of up to CSA2_MAX_B rows then run the
+// Full selection on that view, the rows of a group sharing one workspace.
+__global__ void row_tables_kernel(const csa2_cache c, const int32_t *q_seq, const int64_t *q_pos, int64_t T,
+                                  int64_t *base_v, int32_t *len_v, int32_t *d_err) {
+  pdl_enter();
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < T; r += (int64_t)gridDim.x * blockDim.x) {
+    const int b = q_seq[r];
+    const int64_t p = q_pos[r];
+    int64_t base = 0;
+    int32_t len = 0;
+    if (b < 0 || b >= c.B) set_err(d_err, CSA2_DEVERR_SEQ);
+    else if (p < 0 || p >= (int64_t)c.seq_len[b]) set_err(d_err, CSA2_DEVERR_POS);
+    else { base = c.seq_base[b]; len = (int32_t)(p + 1); }
+    base_v[r] = base;
+    len_v[r] = len;
+  }
+}
+
+constexpr int64_t kChunkRows = CSA2_MAX_B;
+
+size_t chunked_ws_bytes(int64_t T, int64_t max_len, int32_t block, int32_t n_keep) {
+  const int32_t G = (int32_t)std::min<int64_t>(std::max<int64_t>(T, 1), kChunkRows);
+  return align_up((size_t)T * 8) + align_up((size_t)T * 4) + indexer_ws_bytes(G, max_len, block, n_keep);
+}
+
+cudaError_t launch_chunked_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
+                                  const int64_t *q_pos, int64_t T, int block, int n_keep, int topk, int64_t max_len,
+                                  int32_t *pool, int32_t *topk_idx, void *ws, int32_t *d_err, cudaStream_t st) {
+  int64_t *base_v = reinterpret_cast<int64_t *>(ws);
+  int32_t *len_v = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + align_up((size_t)T * 8));
+  void *iws = reinterpret_cast<char *>(len_v) + align_up((size_t)T * 4);
+  const int32_t G = (int32_t)std::min<int64_t>(T, kChunkRows);
+  const IndexerWs iw = indexer_ws_carve(iws, G, max_len, block, n_keep);
+  const unsigned grid = (unsigned)std::min<int64_t>((T + 255) / 256, (int64_t)num_sms() * 4);
+  cudaError_t e = launch_k(row_tables_kernel, dim3(grid), dim3(256), 0, st, 0, c, q_seq, q_pos, T, base_v, len_v, d_err);
+  for (int64_t g0 = 0; e == cudaSuccess && g0 < T; g0 += kChunkRows) {
+    csa2_cache cg = c;
+    cg.B = (int32_t)std::min<int64_t>(kChunkRows, T - g0);
+    cg.seq_base = base_v + g0;
+    cg.seq_len = len_v + g0;
+    e = launch_full_select(cg, q + g0 * kHIdx * kDIdx, w + g0 * kHIdx, block, n_keep, topk, max_len,
+                           pool + g0 * n_keep, topk_idx + g0 * topk, iw, d_err, nullptr, st);
+  }
+  return e;
+}
+
 cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len,
                                float *sigma, double *bound, const IndexerWs &ws, int32_t *d_err,
                                cudaStream_t st) {

@@ -48,6 +48,10 @@ cudaError_t launch_full_select(const csa2_cache &c, const uint16_t *q, const flo
 cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const float *w,
                                   const int32_t *pool, int block, int n_keep, int topk, int64_t max_len,
                                   int32_t *topk_idx, const IndexerWs &ws, int32_t *d_err, cudaStream_t st);
+size_t chunked_ws_bytes(int64_t T, int64_t max_len, int32_t block, int32_t n_keep);
+cudaError_t launch_chunked_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
+                                  const int64_t *q_pos, int64_t T, int block, int n_keep, int topk, int64_t max_len,
+                                  int32_t *pool, int32_t *topk_idx, void *ws, int32_t *d_err, cudaStream_t st);
 cudaError_t launch_verify_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
                                  const int64_t *q_pos, int64_t T, const int32_t *pool, int block, int n_keep, int topk,
                                  int64_t max_len, int32_t *topk_idx, const IndexerWs &ws, int32_t *d_err,

@@ -30,9 +30,9 @@ import torch
 import synth
 from synth.workloads import FULL, REINDEX, REUSE, DecodeWorkload
 
-from . import (Cache, SwaRing, OP_ATTN_DECODE, OP_FULL_SELECT, OP_VERIFY_SELECT, alloc_workspace,
-               indexer_full_select, indexer_reindex_select, indexer_verify_select, kv_append_fp4, sparse_attn_decode,
-               workspace_bytes)
+from . import (Cache, SwaRing, OP_ATTN_DECODE, OP_CHUNKED_SELECT, OP_FULL_SELECT, OP_VERIFY_SELECT,
+               alloc_workspace, indexer_chunked_select, indexer_full_select, indexer_reindex_select,
+               indexer_verify_select, kv_append_fp4, sparse_attn_decode, workspace_bytes)
 
 
 def _to_dev(a: np.ndarray, dtype, device):
@@ -199,9 +199,12 @@ class DecodeRunner:
 
 class ChunkedRunner:
     """The chunked-query workload: many consecutive query rows of one sequence, each with
-    its own causal top-k plus a causal window, attended in one sparse_attn_decode call."""
+    its own causal top-k plus a causal window, attended in one sparse_attn_decode call.
+    ``select()`` computes those top-k lists with the chunked-query indexer (every row's Full
+    selection over the positions up to its own); ``use_indexer=False`` keeps seeded causal
+    lists instead."""
 
-    def __init__(self, wl, device="cuda", chunk: int = 1 << 17):
+    def __init__(self, wl, device="cuda", chunk: int = 1 << 17, use_indexer: bool = True):
         from synth.workloads import ChunkedWorkload
         assert isinstance(wl, ChunkedWorkload)
         self.wl, self.device = wl, device
@@ -237,13 +240,35 @@ class ChunkedRunner:
         self.q_pos = torch.from_numpy(q_pos).to(device)
         self.q_seq = torch.zeros(wl.n_query, dtype=torch.int32, device=device)
         self.topk = torch.from_numpy(synth.causal_topk(s, q_pos, wl.topk)).to(device)
+        # the indexer's inputs and outputs: each row's queries and weights, pool and top-k
+        T = wl.n_query
+        self.qidx = _bf16_dev(np.stack([synth.normals_bf16(s, synth.Stream.QIDX, 0, synth.row_id(r, np.arange(8)), 64)
+                                        for r in range(T)]), device)
+        self.w = _to_dev(np.stack([synth.head_weights(s, 0, r) for r in range(T)]), torch.float32, device)
+        self.block, self.n_keep = 8, 2048
+        self.pool = torch.full((T, self.n_keep), -1, dtype=torch.int32, device=device)
+        self.ws_idx = alloc_workspace(workspace_bytes(OP_CHUNKED_SELECT, max_len=L, block=self.block,
+                                                      n_keep_blocks=self.n_keep, topk=wl.topk, T=T), device)
+        self.positions = int(np.sum(q_pos + 1))          # (row, position) pairs the indexer scores
         q = synth.normals_bf16(s, synth.Stream.Q, 0, np.arange(wl.n_query * wl.H), 128)
         self.q = _bf16_dev(q.reshape(wl.n_query, wl.H, 128), device)
         self.out = torch.empty((wl.n_query, wl.H, 128), dtype=torch.float32, device=device)
         self.lse = torch.empty((wl.n_query, wl.H), dtype=torch.float32, device=device)
         self.ws = alloc_workspace(0, device)
         self.tau = 1.0 / math.sqrt(128.0)
+        if use_indexer:
+            self.select()
         torch.cuda.synchronize()
+
+    def select(self):
+        """The chunked-query indexer: pool and top-k of every row into self.pool / self.topk."""
+        wl = self.wl
+        indexer_chunked_select(self.cache, self.qidx, self.w, self.q_seq, self.q_pos, self.block, self.n_keep, wl.topk,
+                               wl.cache_len, self.pool, self.topk, self.ws_idx, self.d_err)
+
+    def select_flops(self) -> float:
+        """Indexer flops of one select(): 8 heads x 64 dims x 2 per (row, position <= row)."""
+        return 1024.0 * self.positions
 
     def step(self):
         sparse_attn_decode(self.cache, self.swa, self.q, self.q_seq, self.q_pos, self.topk, self.wl.window,

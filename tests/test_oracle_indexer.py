@@ -206,3 +206,26 @@ def test_verify_step_last_row_of_the_full_layer_equals_its_full_top_k():
             for j in range(4):
                 got = res["topk"][l][j]
                 assert np.all(got[got >= 0] <= L - 4 + j)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_chunked_rows_match_brute_force_on_their_prefix(seed):
+    """A chunked-query row at position p: brute force over the first p + 1 positions only,
+    and nothing at or after p + 1 may influence it (later keys are changed to check)."""
+    rng = np.random.default_rng(100 + seed)
+    L = int(rng.integers(20, 70))
+    block = int(rng.choice([1, 2, 4, 8]))
+    n_keep = int(rng.integers(2, 9))
+    topk = int(rng.integers(1, n_keep + 1))
+    codes, scale = _tiny_keys(rng, L)
+    q, w = _tiny_q(rng)
+    qf = bf16_to_f32(q).astype(np.float64).tolist()
+    for p in (0, int(rng.integers(1, L - 1)), L - 1):
+        pool, top, _ = indexer.chunked_select(q, w, codes, scale, p, block, n_keep, topk)
+        bp, bt, _ = bruteforce.select(qf, w.astype(np.float64).tolist(), codes[:p + 1].tolist(),
+                                      scale[:p + 1].astype(np.float64).tolist(), block, n_keep, topk)
+        assert list(pool[pool >= 0]) == bp and list(top[top >= 0]) == bt
+        later = codes.copy()
+        later[p + 1:] = rng.integers(0, 126, size=later[p + 1:].shape)      # finite E4M3 codes
+        pool2, top2, _ = indexer.chunked_select(q, w, later, scale, p, block, n_keep, topk)
+        assert np.array_equal(pool, pool2) and np.array_equal(top, top2)
