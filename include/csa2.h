@@ -345,6 +345,14 @@ int csa2_test_index_scores(const csa2_cache *cache, const uint16_t *q_idx, const
                            int64_t max_len, float *sigma, double *bound, void *ws, size_t ws_bytes,
                            int32_t *d_err, csa2_stream_t stream);
 
+/* Test: the tensor-core scores of T <= CSA2_MAX_B chunked-query rows (rows 16j..16j+15 must
+ * share a session) into sigma [T][max_len] (device floats, positions > q_pos[r] untouched)
+ * and bound [T+1] (device doubles) as for csa2_test_index_scores.  Workspace as for
+ * CSA2_OP_CHUNKED_SELECT with block 8 and n_keep_blocks 1. */
+int csa2_test_chunk_scores(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                           const int64_t *q_pos, int64_t T, int64_t max_len, float *sigma, double *bound, void *ws,
+                           size_t ws_bytes, int32_t *d_err, csa2_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -76,10 +76,11 @@ _attn = _sig("sparse_attn_decode", [_P, _P, _P, _I32, _I64, _P, _P, _P, _I32, _I
 _t_fp4 = _sig("csa2_test_quantize_fp4", [_P, _I64, _P, _P, _P])
 _t_fp8 = _sig("csa2_test_quantize_fp8", [_P, _I64, _I32, _P, _P, _P])
 _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _P, _P])
+_t_cscores = _sig("csa2_test_chunk_scores", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P])
 
 EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "swa_refill_fp8", "indexer_full_select",
             "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select", "indexer_chunked_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
-            "csa2_test_quantize_fp8", "csa2_test_index_scores")
+            "csa2_test_quantize_fp8", "csa2_test_index_scores", "csa2_test_chunk_scores")
 
 
 class Csa2Error(RuntimeError):
@@ -226,6 +227,12 @@ def test_quantize_fp4(x, codes, scales, stream=None):
 def test_quantize_fp8(x, codes, scale, stream=None):
     _check(_t_fp8(_ptr(x), int(x.shape[0]), int(x.shape[1]), _ptr(codes), _ptr(scale), _stream(stream)),
            "csa2_test_quantize_fp8")
+
+
+def test_chunk_scores(cache: Cache, q_idx, w, q_seq, q_pos, max_len, sigma, bound, ws, d_err, stream=None):
+    _check(_t_cscores(ctypes.byref(cache.desc()), _ptr(q_idx), _ptr(w), _ptr(q_seq), _ptr(q_pos), int(q_seq.shape[0]),
+                      int(max_len), _ptr(sigma), _ptr(bound), _ptr(ws), ws.numel(), _ptr(d_err), _stream(stream)),
+           "csa2_test_chunk_scores")
 
 
 def test_index_scores(cache: Cache, q_idx, w, max_len, sigma, bound, ws, d_err, stream=None):

@@ -309,4 +309,18 @@ int csa2_test_index_scores(const csa2_cache *cache, const uint16_t *q_idx, const
   return cuda_status(launch_test_scores(*cache, q_idx, w, max_len, sigma, bound, iw, d_err, (cudaStream_t)stream));
 }
 
+int csa2_test_chunk_scores(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
+                           const int64_t *q_pos, int64_t T, int64_t max_len, float *sigma, double *bound, void *ws,
+                           size_t ws_bytes, int32_t *d_err, csa2_stream_t stream) {
+  if (!cache_ok(cache) || !q_idx || !aligned(q_idx, 16) || !w || !q_seq || !q_pos || !sigma || !bound || !d_err ||
+      T < 1 || T > CSA2_MAX_B)
+    return CSA2_ERR_INVALID_ARG;
+  if (!select_sizes_ok(1, max_len, 8, 1, 1)) return CSA2_ERR_INVALID_ARG;
+  if (!ws || !aligned(ws, 256) || ws_bytes < chunked_ws_bytes(T, max_len, 8, 1)) return CSA2_ERR_WORKSPACE;
+  int st = device_ok();
+  if (st != CSA2_OK) return st;
+  return cuda_status(launch_test_chunk_scores(*cache, q_idx, w, q_seq, q_pos, T, max_len, sigma, bound, ws, d_err,
+                                              (cudaStream_t)stream));
+}
+
 }  // extern "C"

@@ -43,6 +43,17 @@ __device__ __forceinline__ uint32_t f32_to_e2m1_mag(float x) {
   return (uint32_t)__nv_cvt_float_to_fp4(x, __NV_E2M1, cudaRoundNearest) & 7u;
 }
 
+// Power-of-two shift c that brings a query head whose largest |value| is mx into f16 with
+// its maximum in [2^14, 2^15): every value above 2^-29 of the maximum stays exact.
+__device__ __forceinline__ int head_shift(float mx) {
+  if (!(mx > 0.f)) return 0;
+  int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
+  int c = 14 - e;
+  return c < -60 ? -60 : (c > 60 ? 60 : c);
+}
+
+__device__ __forceinline__ float pow2f(int c) { return __uint_as_float((uint32_t)(c + 127) << 23); }
+
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
   __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);

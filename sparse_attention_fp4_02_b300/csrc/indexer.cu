@@ -40,15 +40,6 @@ struct QFrag {
   float wi0, wi1;     // w_h * 2^-c_h for heads 2t, 2t+1
 };
 
-__device__ __forceinline__ int head_shift(float mx) {
-  if (!(mx > 0.f)) return 0;
-  int e = (int)((__float_as_uint(mx) >> 23) & 0xFF) - 127;
-  int c = 14 - e;
-  return c < -60 ? -60 : (c > 60 ? 60 : c);
-}
-
-__device__ __forceinline__ float pow2f(int c) { return __uint_as_float((uint32_t)(c + 127) << 23); }
-
 // 16 query values of head g at dims 16t..16t+15, as float, plus the head's shift
 __device__ __forceinline__ int load_q16(const uint16_t *q_seq, int lane, float v[16]) {
   const int g = lane >> 2, t = lane & 3;
@@ -1609,16 +1600,8 @@ static void launch_positions(IdxArgs &a, cudaStream_t st) {
 }
 
 template <int BLOCK>
-static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_profile *prof, cudaStream_t st) {
+static void launch_finalize(IdxArgs &a, cudaStream_t st) {
   const int B = a.c.B;
-  select_smem_optin<BLOCK>();
-  // inside stream capture a timing event must be an external record node
-  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-  if (prof) cudaStreamIsCapturing(st, &cap);
-  const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
-  if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->start, st, ev_flags);
-  launch_scan<BLOCK, true>(a, max_len, st);
-  if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
   const int64_t nbm = a.ws.nbm;
   // pool and top-k positions in separate CTAs while both fit in one wave (one CTA per SM)
   const dim3 fin((unsigned)B, 2 * B <= num_sms() ? 2u : 1u);
@@ -1629,6 +1612,35 @@ static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_prof
     launch_k(collect_kernel<BLOCK>, cg, dim3(256), 0, st, 0, a);
     launch_k(finalize_blocks_kernel<BLOCK, false>, fin, dim3(kSelCta), kFinalizeSmemCand, st, 0, a);
   }
+}
+
+template <int BLOCK>
+static cudaError_t full_select_impl(IdxArgs &a, int64_t max_len, const csa2_profile *prof, cudaStream_t st) {
+  select_smem_optin<BLOCK>();
+  // inside stream capture a timing event must be an external record node
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (prof) cudaStreamIsCapturing(st, &cap);
+  const unsigned ev_flags = cap == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+  if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->start, st, ev_flags);
+  launch_scan<BLOCK, true>(a, max_len, st);
+  if (prof) cudaEventRecordWithFlags((cudaEvent_t)prof->stop, st, ev_flags);
+  launch_finalize<BLOCK>(a, st);
+  return cudaGetLastError();
+}
+
+// One group of chunked-query rows: rows in uniform groups of 16 are scored on the tensor
+// cores, the others by the one-query scan (which sees them through len_scan), then the
+// usual finalize on the true row view.
+template <int BLOCK>
+static cudaError_t chunked_group_impl(IdxArgs &a, const int32_t *len_scan, const CqArgs &cq, int64_t max_len,
+                                      cudaStream_t st) {
+  select_smem_optin<BLOCK>();
+  cudaError_t e = launch_chunk_scores_tc(cq, BLOCK, st);
+  if (e != cudaSuccess) return e;
+  IdxArgs as = a;
+  as.c.seq_len = len_scan;
+  launch_scan<BLOCK, true>(as, max_len, st);
+  launch_finalize<BLOCK>(a, st);
   return cudaGetLastError();
 }
 
@@ -1727,21 +1739,41 @@ cudaError_t launch_verify_select(const csa2_cache &c, const uint16_t *q, const f
 
 // Chunked queries: every query row gets the Full selection over its session's positions up
 // to its own.  A small kernel turns (session, position) into a per-row view of the cache
-// (the session's base, length position + 1); groups of up to CSA2_MAX_B rows then run the
-// Full selection on that view, the rows of a group sharing one workspace.
+// (the session's base, length position + 1) and marks the rows whose group of 16 shares one
+// session: those are scored on the tensor cores, the rest by the one-query scan (which sees
+// them through len_scan).  Groups of up to CSA2_MAX_B rows then run the selection on that
+// view, the rows of a group sharing one workspace.
 __global__ void row_tables_kernel(const csa2_cache c, const int32_t *q_seq, const int64_t *q_pos, int64_t T,
-                                  int64_t *base_v, int32_t *len_v, int32_t *d_err) {
+                                  int64_t max_len, int64_t *base_v, int32_t *len_v, int32_t *len_scan,
+                                  int32_t *d_err) {
   pdl_enter();
-  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < T; r += (int64_t)gridDim.x * blockDim.x) {
-    const int b = q_seq[r];
-    const int64_t p = q_pos[r];
+  const int lane = threadIdx.x & 31;
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;            // a multiple of 32
+  for (int64_t r0 = (int64_t)blockIdx.x * blockDim.x + (threadIdx.x & ~31); r0 < T; r0 += stride) {
+    const int64_t r = r0 + lane;
     int64_t base = 0;
     int32_t len = 0;
-    if (b < 0 || b >= c.B) set_err(d_err, CSA2_DEVERR_SEQ);
-    else if (p < 0 || p >= (int64_t)c.seq_len[b]) set_err(d_err, CSA2_DEVERR_POS);
-    else { base = c.seq_base[b]; len = (int32_t)(p + 1); }
-    base_v[r] = base;
-    len_v[r] = len;
+    if (r < T) {
+      const int b = q_seq[r];
+      const int64_t p = q_pos[r];
+      if (b < 0 || b >= c.B) {
+        set_err(d_err, CSA2_DEVERR_SEQ);
+      } else if (p < 0 || p >= (int64_t)c.seq_len[b]) {
+        set_err(d_err, CSA2_DEVERR_POS);
+      } else if (p + 1 > max_len || c.seq_base[b] < 0 || c.seq_base[b] + c.seq_len[b] > c.T_cap) {
+        set_err(d_err, CSA2_DEVERR_LEN);                            // the row reads nothing
+      } else {
+        base = c.seq_base[b];
+        len = (int32_t)(p + 1);
+      }
+      base_v[r] = base;
+      len_v[r] = len;
+    }
+    // r0 is a multiple of 32: lanes 0-15 and 16-31 each hold one group of 16 rows
+    const int64_t b0 = __shfl_sync(0xffffffffu, base, lane & 16);
+    const unsigned same = __ballot_sync(0xffffffffu, r >= T || base == b0);
+    const bool uniform = ((same >> (lane & 16)) & 0xFFFFu) == 0xFFFFu;
+    if (r < T) len_scan[r] = uniform ? 0 : len;
   }
 }
 
@@ -1749,7 +1781,7 @@ constexpr int64_t kChunkRows = CSA2_MAX_B;
 
 size_t chunked_ws_bytes(int64_t T, int64_t max_len, int32_t block, int32_t n_keep) {
   const int32_t G = (int32_t)std::min<int64_t>(std::max<int64_t>(T, 1), kChunkRows);
-  return align_up((size_t)T * 8) + align_up((size_t)T * 4) + indexer_ws_bytes(G, max_len, block, n_keep);
+  return align_up((size_t)T * 8) + 2 * align_up((size_t)T * 4) + indexer_ws_bytes(G, max_len, block, n_keep);
 }
 
 cudaError_t launch_chunked_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
@@ -1757,20 +1789,63 @@ cudaError_t launch_chunked_select(const csa2_cache &c, const uint16_t *q, const 
                                   int32_t *pool, int32_t *topk_idx, void *ws, int32_t *d_err, cudaStream_t st) {
   int64_t *base_v = reinterpret_cast<int64_t *>(ws);
   int32_t *len_v = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + align_up((size_t)T * 8));
-  void *iws = reinterpret_cast<char *>(len_v) + align_up((size_t)T * 4);
+  int32_t *len_scan = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(len_v) + align_up((size_t)T * 4));
+  void *iws = reinterpret_cast<char *>(len_scan) + align_up((size_t)T * 4);
   const int32_t G = (int32_t)std::min<int64_t>(T, kChunkRows);
   const IndexerWs iw = indexer_ws_carve(iws, G, max_len, block, n_keep);
   const unsigned grid = (unsigned)std::min<int64_t>((T + 255) / 256, (int64_t)num_sms() * 4);
-  cudaError_t e = launch_k(row_tables_kernel, dim3(grid), dim3(256), 0, st, 0, c, q_seq, q_pos, T, base_v, len_v, d_err);
+  cudaError_t e = launch_k(row_tables_kernel, dim3(grid), dim3(256), 0, st, 0, c, q_seq, q_pos, T, max_len, base_v,
+                           len_v, len_scan, d_err);
   for (int64_t g0 = 0; e == cudaSuccess && g0 < T; g0 += kChunkRows) {
     csa2_cache cg = c;
     cg.B = (int32_t)std::min<int64_t>(kChunkRows, T - g0);
     cg.seq_base = base_v + g0;
     cg.seq_len = len_v + g0;
-    e = launch_full_select(cg, q + g0 * kHIdx * kDIdx, w + g0 * kHIdx, block, n_keep, topk, max_len,
-                           pool + g0 * n_keep, topk_idx + g0 * topk, iw, d_err, nullptr, st);
+    e = zero_ws(iw, st);
+    if (e != cudaSuccess) break;
+    IdxArgs a = make_args(cg, q + g0 * kHIdx * kDIdx, w + g0 * kHIdx, max_len, n_keep, topk, iw, d_err);
+    a.pool_out = pool + g0 * n_keep;
+    a.pool_in = a.pool_out;
+    a.topk_out = topk_idx + g0 * topk;
+    CqArgs cq;
+    cq.ik_codes = c.ik_codes; cq.ik_scale = c.ik_scale;
+    cq.base_v = base_v + g0; cq.len_v = len_v + g0;
+    cq.q = a.q; cq.w = a.w; cq.n = cg.B; cq.ws = iw; cq.d_err = d_err;
+    const int32_t *ls = len_scan + g0;
+    auto run = [&]() -> cudaError_t { CSA2_DISPATCH_BLOCK(block, chunked_group_impl<BL>(a, ls, cq, max_len, st)); };
+    e = run();
   }
   return e;
+}
+
+// Test: the tensor-core scores of up to CSA2_MAX_B chunked-query rows (each row's group of
+// 16 must share a session) into sigma [T][max_len], with the per-row bound as for the scan.
+cudaError_t launch_test_chunk_scores(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
+                                     const int64_t *q_pos, int64_t T, int64_t max_len, float *sigma, double *bound,
+                                     void *ws, int32_t *d_err, cudaStream_t st) {
+  int64_t *base_v = reinterpret_cast<int64_t *>(ws);
+  int32_t *len_v = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(ws) + align_up((size_t)T * 8));
+  int32_t *len_scan = reinterpret_cast<int32_t *>(reinterpret_cast<char *>(len_v) + align_up((size_t)T * 4));
+  void *iws = reinterpret_cast<char *>(len_scan) + align_up((size_t)T * 4);
+  IndexerWs iw = indexer_ws_carve(iws, (int32_t)T, max_len, 8, 1);
+  cudaError_t e = launch_k(row_tables_kernel, dim3(1), dim3(1024), 0, st, 0, c, q_seq, q_pos, T, max_len, base_v,
+                           len_v, len_scan, d_err);
+  if (e == cudaSuccess) e = zero_ws(iw, st);
+  if (e != cudaSuccess) return e;
+  iw.sigma = sigma;
+  iw.sigma_stride = max_len;
+  CqArgs cq;
+  cq.ik_codes = c.ik_codes; cq.ik_scale = c.ik_scale;
+  cq.base_v = base_v; cq.len_v = len_v; cq.q = q; cq.w = w; cq.n = (int)T; cq.ws = iw; cq.d_err = d_err;
+  e = launch_chunk_scores_tc(cq, 8, st);
+  if (e != cudaSuccess) return e;
+  csa2_cache cv = c;
+  cv.B = (int32_t)T;
+  cv.seq_base = base_v;
+  cv.seq_len = len_v;
+  IdxArgs a = make_args(cv, q, w, max_len, 1, 1, iw, d_err);
+  bound_kernel<<<(unsigned)T, 32, 0, st>>>(a, bound);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_test_scores(const csa2_cache &c, const uint16_t *q, const float *w, int64_t max_len,

@@ -1,0 +1,309 @@
+// Chunked-query indexer scores on the 5th-generation tensor cores (tcgen05 + TMEM).
+//
+// Method: the Full layer's indexer score (origotech.dev deep dive, subsection "Compressed
+// Sparse Attention 2(CSA2)"), sigma_t = s_t * sum_h w_h * max(q_h . k_t, 0), for many query
+// rows of one session at once.  Sixteen rows share every key, so their 16 x 8 head queries
+// form the N = 128 side of one dense contraction per tile of 128 keys:
+//   D = K Q^T      (M = 128 keys, N = 16 rows x 8 heads, K = 64 dims)
+// The E4M3 keys are converted exactly to f16 into shared-memory core matrices, the queries
+// are scaled per (row, head) by the same power of two as in the one-query scan (so the same
+// certified error bound holds), D accumulates in TMEM, and the epilogue (thread <-> key,
+// eight rows per thread) forms ReLU * w, the key scale, the block maxima and their
+// histogram, and stores every position's score for the exact selection that follows.
+// A row only counts the positions up to its own (its length in the row view).
+//
+// Pipeline per CTA (persistent over (group, tile) items): the raw bytes of the next tile
+// are loaded into registers while the current tile is converted, one thread issues the
+// MMAs into one of two TMEM accumulators, and the epilogue of the previous tile runs while
+// the tensor cores work on the current one.
+#include <cfloat>
+
+#include "common.cuh"
+#include "launch.h"
+#include "tcgen05.cuh"
+
+namespace csa2 {
+
+constexpr int kCqRows = 16;                                // query rows per group
+constexpr int kCqKeys = 128;                               // keys per tile (MMA M)
+constexpr int kCqN = kCqRows * kHIdx;                      // MMA N = 128
+constexpr int kCqThreads = 256;
+constexpr int kCqCols = 2 * kCqN;                          // TMEM: two accumulators
+constexpr int kCqTileBytes = kCqKeys * kDIdx * 2;          // 16 KB of f16 keys
+constexpr int kCqQ = 0;                                    // Q: 128 x 64 f16, 16 KB
+constexpr int kCqK = kCqQ + kCqN * kDIdx * 2;              // two key tiles
+constexpr int kCqSmem = kCqK + 2 * kCqTileBytes;           // 48 KB
+constexpr int kCqSmemLaunch = 80 * 1024;                   // at most two CTAs per SM: 2 x 256 TMEM columns
+constexpr int kCqMaxGroups = CSA2_MAX_B / kCqRows;
+constexpr int kCqRowGroupBytes = (kDIdx / 8) * 128;        // 8 rows x 64 dims: 8 core matrices
+static_assert(kCqSmem <= kCqSmemLaunch, "layout");
+static_assert(kCqN == 128, "one accumulator is 128 columns");
+
+// Byte offset of (row n, dims 8kg..8kg+7) in a K-major no-swizzle operand of 64 dims.
+__device__ __forceinline__ int cq_off(int n, int kg) { return (n >> 3) * kCqRowGroupBytes + kg * 128 + (n & 7) * 16; }
+
+// A group of rows is scored here when all its rows share one session (one base).
+__device__ __forceinline__ bool cq_uniform(const CqArgs &a, int g, int64_t &base, int32_t &maxlen) {
+  const int r0 = g * kCqRows, r1 = min(a.n, r0 + kCqRows);
+  base = a.base_v[r0];
+  maxlen = 0;
+  bool uni = true;
+  for (int r = r0; r < r1; ++r) {
+    uni = uni && a.base_v[r] == base;
+    maxlen = max(maxlen, a.len_v[r]);
+  }
+  return uni;
+}
+
+template <int BLOCK>
+__global__ void __launch_bounds__(kCqThreads, 2) chunk_scores_tc_kernel(const __grid_constant__ CqArgs a) {
+  extern __shared__ __align__(1024) uint8_t s_dyn[];
+  __shared__ __align__(8) uint64_t s_mbar[2];
+  __shared__ uint32_t s_tmem;
+  __shared__ int64_t s_first[kCqMaxGroups + 1];              // first item of each group
+  __shared__ int64_t s_base[kCqMaxGroups];
+  __shared__ int32_t s_maxlen[kCqMaxGroups];
+  __shared__ float s_wi[kCqRows][kHIdx];                      // w * 2^-c of the current group
+  __shared__ int32_t s_len[kCqRows];                          // lengths of the current group's rows
+  pdl_enter();
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int ngroups = (a.n + kCqRows - 1) / kCqRows;
+
+  // ---- items: (group, tile), group-major; a group that is not uniform has none
+  if (tid < ngroups) {
+    int64_t base;
+    int32_t ml;
+    const bool uni = cq_uniform(a, tid, base, ml);
+    s_base[tid] = base;
+    s_maxlen[tid] = uni ? ml : 0;
+  }
+  if (tid == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&s_mbar[0])));
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&s_mbar[1])));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int64_t run = 0;
+    for (int g = 0; g < ngroups; ++g) { s_first[g] = run; run += (s_maxlen[g] + kCqKeys - 1) / kCqKeys; }
+    s_first[ngroups] = run;
+  }
+  __syncthreads();
+  const int64_t total = s_first[ngroups];
+  const int64_t it0 = total * blockIdx.x / gridDim.x, it1 = total * (blockIdx.x + 1) / gridDim.x;
+  if (it0 >= it1) return;                                     // uniform across the CTA
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&s_tmem)),
+                 "r"(kCqCols));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = s_tmem;
+  const uint32_t idesc = umma_idesc(kCqKeys, kCqN, 0, 0);
+  uint8_t *qs = s_dyn + kCqQ;
+  const uint32_t qs_a = smem_addr(qs), ks_a = smem_addr(s_dyn + kCqK);
+
+  auto group_of = [&](int64_t item) {                          // s_first[g] <= item < s_first[g + 1]
+    int lo = 0, hi = ngroups;
+    while (hi - lo > 1) { const int mid = (lo + hi) >> 1; if (s_first[mid] <= item) lo = mid; else hi = mid; }
+    while (s_first[lo + 1] == s_first[lo]) ++lo;
+    return lo;
+  };
+
+  // converter role: key km of a tile, dims 32 dh .. 32 dh + 31 (the same thread runs the
+  // epilogue of key km: warps 0-3 rows 0-7, warps 4-7 rows 8-15 of the group)
+  const int km = tid & (kCqKeys - 1), dh = tid >> 7;
+  const int eh = warp >> 2;                                   // epilogue rows 8 eh .. 8 eh + 7
+  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
+  uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;                  // raw codes of the next tile's key
+  float xs = 0.f;                                             // its scale (0: beyond every row)
+  auto fetch = [&](int64_t item) {
+    const int g = group_of(item);
+    const int64_t kk = (item - s_first[g]) * kCqKeys + km;
+    const bool v = kk < s_maxlen[g];
+    const int64_t row = s_base[g] + (v ? kk : 0);
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.ik_codes + row * kDIdx + 32 * dh);
+    x0 = v ? ld_nc16(reinterpret_cast<const uint8_t *>(src)) : make_uint4(0, 0, 0, 0);
+    x1 = v ? ld_nc16(reinterpret_cast<const uint8_t *>(src + 1)) : make_uint4(0, 0, 0, 0);
+    xs = v ? __ldg(a.ik_scale + row) : 0.f;
+  };
+
+  float smx[8];                                               // per row: largest valid key scale seen
+#pragma unroll
+  for (int j = 0; j < 8; ++j) smx[j] = 0.f;
+  int cur_g = -1;
+  auto flush_smax = [&]() {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float m = warp_max(smx[j]);
+      const int r = cur_g * kCqRows + 8 * eh + j;
+      if (lane == 0 && r < a.n && m > 0.f) atomicMax(&a.ws.smax[r], __float_as_uint(m));
+      smx[j] = 0.f;
+    }
+  };
+
+  uint32_t ph0 = 0, ph1 = 0;
+  bool dead = false;                                          // a wait ran out (uniform after a CTA vote)
+  // the pending epilogue: its tile, buffer and key scale
+  bool pend = false;
+  int64_t pend_tile = 0;
+  int pend_buf = 0;
+  float pend_ks = 0.f;
+  auto epilogue = [&]() {
+    const uint32_t mb = smem_addr(&s_mbar[pend_buf]);
+    // warp-uniform: the TMEM loads below need every lane of the warp
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(mb, pend_buf ? ph1 : ph0));
+    if (pend_buf) ph1 ^= 1u; else ph0 ^= 1u;
+    tc_fence_after();
+    if (!ok) { dead = true; if (lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT); return; }
+    float v[64];
+    {
+      float t0[32], t1[32];
+      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eh, t0);
+      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eh + 32, t1);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) { v[i] = t0[i]; v[32 + i] = t1[i]; }
+    }
+    const int em = 32 * (warp & 3) + lane;                    // == km
+    const int64_t kk = pend_tile * kCqKeys + em;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int jr = 8 * eh + j;
+      const int r = cur_g * kCqRows + jr;
+      float acc = 0.f;
+#pragma unroll
+      for (int h = 0; h < kHIdx; ++h) acc += fmaxf(v[8 * j + h], 0.f) * s_wi[jr][h];
+      float o = acc * pend_ks;
+      o = o > 0.f ? o : 0.f;                                  // also maps NaN and -0 to +0
+      const bool valid = kk < s_len[jr];
+      if (valid) a.ws.sigma[(int64_t)r * a.ws.sigma_stride + kk] = o;
+      smx[j] = fmaxf(smx[j], valid ? pend_ks : 0.f);
+      float m = valid ? o : 0.f;
+#pragma unroll
+      for (int s = 1; s < BLOCK; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+      if ((em % BLOCK) == 0 && valid) {
+        a.ws.bmax[(int64_t)r * a.ws.nbm + kk / BLOCK] = m;
+        atomicAdd(&a.ws.hist[(int64_t)r * kHistBins + min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)],
+                  1u);
+      }
+    }
+  };
+
+  fetch(it0);
+  for (int64_t it = it0; it < it1; ++it) {
+    const int g = group_of(it);
+    const int buf = (int)((it - it0) & 1);
+    if (g != cur_g) {
+      // the previous group's last tile completes before its queries are replaced
+      if (pend) { epilogue(); pend = false; }
+      if (cur_g >= 0) flush_smax();
+      if (__syncthreads_or(dead)) break;
+      // queries of group g: (row jr, head h) = MMA column n = 8 jr + h; two threads per pair
+      {
+        const int pair = tid >> 1, half = tid & 1;
+        const int jr = pair >> 3, h = pair & 7;
+        const int r = g * kCqRows + jr;
+        const bool rv = r < a.n;
+        uint32_t wq[16];
+        float mx = 0.f;
+        if (rv) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * kHIdx + h) * kDIdx + 32 * half);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const uint4 u = __ldg(src + i);
+            wq[4 * i] = u.x; wq[4 * i + 1] = u.y; wq[4 * i + 2] = u.z; wq[4 * i + 3] = u.w;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) wq[i] = 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(wq[i] & 0xFFFFu)), fabsf(bf16_to_f32(wq[i] >> 16))));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        const int c = head_shift(mx);
+        const float sc = pow2f(c);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {                         // dims 32 half + 8 i .. + 7
+          uint32_t o4[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const uint32_t wv = wq[4 * i + e];
+            o4[e] = pack_f16x2(bf16_to_f32(wv & 0xFFFFu) * sc, bf16_to_f32(wv >> 16) * sc);
+          }
+          *reinterpret_cast<uint4 *>(qs + cq_off(pair, 4 * half + i)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+        }
+        if (half == 0) s_wi[jr][h] = rv ? __ldg(a.w + (int64_t)r * kHIdx + h) * pow2f(-c) : 0.f;
+        if (tid < kCqRows) s_len[tid] = (g * kCqRows + tid < a.n) ? a.len_v[g * kCqRows + tid] : 0;
+      }
+      cur_g = g;
+    }
+    // ---- this tile's keys, exactly to f16, into its buffer; then the next tile's loads
+    {
+      uint8_t *kb = s_dyn + kCqK + buf * kCqTileBytes;
+      const uint32_t w8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {                           // dims 32 dh + 8 i .. + 7
+        const uint32_t lo = w8[2 * i], hi = w8[2 * i + 1];
+        *reinterpret_cast<uint4 *>(kb + cq_off(km, 4 * dh + i)) =
+            make_uint4(e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
+                       e4m3x2_to_f16x2(hi >> 16));
+      }
+    }
+    const float cur_ks = xs;
+    if (it + 1 < it1) fetch(it + 1);
+    fence_async_smem();
+    tc_fence_before();
+    if (__syncthreads_or(dead)) break;
+    tc_fence_after();
+    if (tid == 0) {
+      const uint32_t kb_a = ks_a + buf * kCqTileBytes;
+#pragma unroll
+      for (int s = 0; s < kDIdx / 16; ++s)
+        umma_f16(tmem + buf * kCqN, umma_desc(kb_a + 256 * s, 128, kCqRowGroupBytes),
+                 umma_desc(qs_a + 256 * s, 128, kCqRowGroupBytes), idesc, s > 0);
+      umma_commit(smem_addr(&s_mbar[buf]));
+    }
+    __syncwarp();
+    if (pend) epilogue();
+    pend = true;
+    pend_tile = it - s_first[g];
+    pend_buf = buf;
+    pend_ks = cur_ks;
+  }
+  dead = __syncthreads_or(dead);
+  if (pend && !dead) epilogue();
+  dead = __syncthreads_or(dead);
+  if (cur_g >= 0 && !dead) flush_smax();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kCqCols));
+}
+
+template <int BLOCK>
+static cudaError_t launch_cq(const CqArgs &a, cudaStream_t st) {
+  static bool optin = false;
+  if (!optin) {
+    cudaFuncSetAttribute(chunk_scores_tc_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCqSmemLaunch);
+    optin = true;
+  }
+  return launch_k(chunk_scores_tc_kernel<BLOCK>, dim3((unsigned)(2 * num_sms())), dim3(kCqThreads), kCqSmemLaunch, st,
+                  0, a);
+}
+
+cudaError_t launch_chunk_scores_tc(const CqArgs &a, int block, cudaStream_t st) {
+  switch (block) {
+    case 1: return launch_cq<1>(a, st);
+    case 2: return launch_cq<2>(a, st);
+    case 4: return launch_cq<4>(a, st);
+    case 8: return launch_cq<8>(a, st);
+    case 16: return launch_cq<16>(a, st);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace csa2

@@ -48,6 +48,23 @@ cudaError_t launch_full_select(const csa2_cache &c, const uint16_t *q, const flo
 cudaError_t launch_reindex_select(const csa2_cache &c, const uint16_t *q, const float *w,
                                   const int32_t *pool, int block, int n_keep, int topk, int64_t max_len,
                                   int32_t *topk_idx, const IndexerWs &ws, int32_t *d_err, cudaStream_t st);
+// Chunked-query scores on the tensor cores: rows [0, n) of a row view of the cache; groups
+// of 16 rows sharing one base are scored, the others are left to the one-query scan.
+struct CqArgs {
+  const uint8_t *ik_codes;
+  const float *ik_scale;
+  const int64_t *base_v;     // [n] each row's session base
+  const int32_t *len_v;      // [n] each row's length (position + 1; 0: none)
+  const uint16_t *q;         // [n][8][64] bf16
+  const float *w;            // [n][8]
+  int n;
+  IndexerWs ws;              // carved for >= n rows
+  int32_t *d_err;
+};
+cudaError_t launch_chunk_scores_tc(const CqArgs &a, int block, cudaStream_t st);
+cudaError_t launch_test_chunk_scores(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
+                                     const int64_t *q_pos, int64_t T, int64_t max_len, float *sigma, double *bound,
+                                     void *ws, int32_t *d_err, cudaStream_t st);
 size_t chunked_ws_bytes(int64_t T, int64_t max_len, int32_t block, int32_t n_keep);
 cudaError_t launch_chunked_select(const csa2_cache &c, const uint16_t *q, const float *w, const int32_t *q_seq,
                                   const int64_t *q_pos, int64_t T, int block, int n_keep, int topk, int64_t max_len,

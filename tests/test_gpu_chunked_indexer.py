@@ -91,3 +91,36 @@ def test_chunk_of_4096_queries_over_a_262144_token_cache():
     L, T = 262144, 4096
     q_pos = np.arange(L - T, L, dtype=np.int64)
     assert compare([L], np.zeros(T, np.int32), q_pos, rows=[0, 2047, 4095]) == 0
+
+
+def test_tensor_core_scores_obey_the_error_bound():
+    """The tcgen05 scores of 48 rows (three groups of 16) against the oracle's exact scores:
+    |approx - exact| <= E_row + r * approx at every position up to the row's own; positions
+    after it are left untouched."""
+    L = 40000
+    cache, ref = fill([L], seed=1)
+    q_pos = np.concatenate([np.arange(L - 16, L), np.arange(100, 116), np.arange(20000, 20016)]).astype(np.int64)
+    T = q_pos.shape[0]
+    q, w = row_queries(T, layer=11, seed=1)
+    sigma = torch.full((T, L), -1.0, dtype=torch.float32, device="cuda")
+    bound = torch.zeros(T + 1, dtype=torch.float64, device="cuda")
+    ws = csa2.alloc_workspace(csa2.workspace_bytes(csa2.OP_CHUNKED_SELECT, max_len=L, block=8, n_keep_blocks=1,
+                                                   topk=1, T=T))
+    d_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    csa2.test_chunk_scores(cache, dev_bf16(q), dev(w), dev(np.zeros(T, np.int32)), dev(q_pos), L, sigma, bound, ws,
+                           d_err)
+    torch.cuda.synchronize()
+    assert int(d_err.item()) == 0
+    sg, bd = host(sigma).astype(np.float64), host(bound)
+    rr = bd[T]
+    _, _, ic, isc = ref[0]
+    worst = 0.0
+    for r in range(T):
+        p = int(q_pos[r])
+        exact = ix.scores(q[r], w[r], ic[:p + 1], isc[:p + 1])
+        err = np.abs(sg[r, :p + 1] - exact)
+        lim = bd[r] + rr * sg[r, :p + 1]
+        assert np.all(err <= lim), f"row {r}: bound violated: {np.max(err / lim)}"
+        assert np.all(sg[r, p + 1:] == -1.0)
+        worst = max(worst, float(np.max(err / lim)))
+    print(f"max |approx - exact| / bound = {worst:.3e}")
