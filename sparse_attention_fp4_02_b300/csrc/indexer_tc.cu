@@ -8,7 +8,7 @@
 // The E4M3 keys are converted exactly to f16 into shared-memory core matrices, the queries
 // are scaled per (row, head) by the same power of two as in the one-query scan (so the same
 // certified error bound holds), D accumulates in TMEM, and the epilogue (thread <-> key,
-// eight rows per thread) forms ReLU * w, the key scale, the block maxima and their
+// four rows per thread) forms ReLU * w, the key scale, the block maxima and their
 // histogram, and stores every position's score for the exact selection that follows.
 // A row only counts the positions up to its own (its length in the row view).
 //
@@ -27,13 +27,13 @@ namespace csa2 {
 constexpr int kCqRows = 16;                                // query rows per group
 constexpr int kCqKeys = 128;                               // keys per tile (MMA M)
 constexpr int kCqN = kCqRows * kHIdx;                      // MMA N = 128
-constexpr int kCqThreads = 256;
+constexpr int kCqThreads = 512;                            // 16 warps: 4 per TMEM lane quarter
 constexpr int kCqCols = 2 * kCqN;                          // TMEM: two accumulators
 constexpr int kCqTileBytes = kCqKeys * kDIdx * 2;          // 16 KB of f16 keys
 constexpr int kCqQ = 0;                                    // Q: 128 x 64 f16, 16 KB
 constexpr int kCqK = kCqQ + kCqN * kDIdx * 2;              // two key tiles
 constexpr int kCqSmem = kCqK + 2 * kCqTileBytes;           // 48 KB
-constexpr int kCqSmemLaunch = 80 * 1024;                   // at most two CTAs per SM: 2 x 256 TMEM columns
+constexpr int kCqSmemLaunch = 80 * 1024;                   // one CTA per SM (also set by its registers)
 constexpr int kCqMaxGroups = CSA2_MAX_B / kCqRows;
 constexpr int kCqRowGroupBytes = (kDIdx / 8) * 128;        // 8 rows x 64 dims: 8 core matrices
 static_assert(kCqSmem <= kCqSmemLaunch, "layout");
@@ -56,7 +56,7 @@ __device__ __forceinline__ bool cq_uniform(const CqArgs &a, int g, int64_t &base
 }
 
 template <int BLOCK>
-__global__ void __launch_bounds__(kCqThreads, 2) chunk_scores_tc_kernel(const __grid_constant__ CqArgs a) {
+__global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __grid_constant__ CqArgs a) {
   extern __shared__ __align__(1024) uint8_t s_dyn[];
   __shared__ __align__(8) uint64_t s_mbar[2];
   __shared__ uint32_t s_tmem;
@@ -106,40 +106,53 @@ __global__ void __launch_bounds__(kCqThreads, 2) chunk_scores_tc_kernel(const __
   uint8_t *qs = s_dyn + kCqQ;
   const uint32_t qs_a = smem_addr(qs), ks_a = smem_addr(s_dyn + kCqK);
 
-  auto group_of = [&](int64_t item) {                          // s_first[g] <= item < s_first[g + 1]
-    int lo = 0, hi = ngroups;
-    while (hi - lo > 1) { const int mid = (lo + hi) >> 1; if (s_first[mid] <= item) lo = mid; else hi = mid; }
+  // item cursors (group, tile): one for the tile being issued, one for the loads ahead
+  int g_it, g_ft;
+  int64_t t_it, t_ft;
+  {
+    int lo = 0, hi = ngroups;                                   // s_first[lo] <= it0 < s_first[lo + 1]
+    while (hi - lo > 1) { const int mid = (lo + hi) >> 1; if (s_first[mid] <= it0) lo = mid; else hi = mid; }
     while (s_first[lo + 1] == s_first[lo]) ++lo;
-    return lo;
+    g_it = g_ft = lo;
+    t_it = t_ft = it0 - s_first[lo];
+  }
+  auto advance = [&](int &g, int64_t &t) {
+    if (++t == s_first[g + 1] - s_first[g]) {
+      t = 0;
+      do { ++g; } while (g < ngroups && s_first[g + 1] == s_first[g]);
+    }
   };
 
-  // converter role: key km of a tile, dims 32 dh .. 32 dh + 31 (the same thread runs the
-  // epilogue of key km: warps 0-3 rows 0-7, warps 4-7 rows 8-15 of the group)
-  const int km = tid & (kCqKeys - 1), dh = tid >> 7;
-  const int eh = warp >> 2;                                   // epilogue rows 8 eh .. 8 eh + 7
+  // converter role: key km of a tile, dims 16 dq .. 16 dq + 15; the same thread runs the
+  // epilogue of key km for rows 4 eq .. 4 eq + 3 of the group (TMEM columns 32 eq ..)
+  const int km = tid & (kCqKeys - 1), dq = tid >> 7;
+  const int eq = warp >> 2;
   const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;
-  uint4 x0 = make_uint4(0, 0, 0, 0), x1 = x0;                  // raw codes of the next tile's key
+  uint4 x0 = make_uint4(0, 0, 0, 0);                         // raw codes of the next tile's key
   float xs = 0.f;                                             // its scale (0: beyond every row)
-  auto fetch = [&](int64_t item) {
-    const int g = group_of(item);
-    const int64_t kk = (item - s_first[g]) * kCqKeys + km;
-    const bool v = kk < s_maxlen[g];
-    const int64_t row = s_base[g] + (v ? kk : 0);
-    const uint4 *src = reinterpret_cast<const uint4 *>(a.ik_codes + row * kDIdx + 32 * dh);
-    x0 = v ? ld_nc16(reinterpret_cast<const uint8_t *>(src)) : make_uint4(0, 0, 0, 0);
-    x1 = v ? ld_nc16(reinterpret_cast<const uint8_t *>(src + 1)) : make_uint4(0, 0, 0, 0);
+  auto fetch = [&]() {                                        // the tile at the load cursor
+    const int64_t kk = t_ft * kCqKeys + km;
+    const bool v = kk < s_maxlen[g_ft];
+    const int64_t row = s_base[g_ft] + (v ? kk : 0);
+    x0 = v ? ld_nc16(a.ik_codes + row * kDIdx + 16 * dq) : make_uint4(0, 0, 0, 0);
     xs = v ? __ldg(a.ik_scale + row) : 0.f;
   };
 
-  float smx[8];                                               // per row: largest valid key scale seen
+  // the current group's rows of this thread: weights, lengths, score rows
+  float wr[4][kHIdx] = {};
+  int32_t lenr[4];
+  float *rowp[4];
+  float *bmaxp[4];
+  uint32_t *histp[4];
+  float smx[4];                                               // per row: largest valid key scale seen
 #pragma unroll
-  for (int j = 0; j < 8; ++j) smx[j] = 0.f;
+  for (int j = 0; j < 4; ++j) { smx[j] = 0.f; lenr[j] = 0; rowp[j] = a.ws.sigma; bmaxp[j] = a.ws.bmax; histp[j] = a.ws.hist; }
   int cur_g = -1;
   auto flush_smax = [&]() {
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
+    for (int j = 0; j < 4; ++j) {
       const float m = warp_max(smx[j]);
-      const int r = cur_g * kCqRows + 8 * eh + j;
+      const int r = cur_g * kCqRows + 4 * eq + j;
       if (lane == 0 && r < a.n && m > 0.f) atomicMax(&a.ws.smax[r], __float_as_uint(m));
       smx[j] = 0.f;
     }
@@ -154,111 +167,134 @@ __global__ void __launch_bounds__(kCqThreads, 2) chunk_scores_tc_kernel(const __
   float pend_ks = 0.f;
   auto epilogue = [&]() {
     const uint32_t mb = smem_addr(&s_mbar[pend_buf]);
-    // warp-uniform: the TMEM loads below need every lane of the warp
+    // warp-uniform: the TMEM load below needs every lane of the warp
     const bool ok = __all_sync(0xffffffffu, mbar_wait(mb, pend_buf ? ph1 : ph0));
     if (pend_buf) ph1 ^= 1u; else ph0 ^= 1u;
     tc_fence_after();
     if (!ok) { dead = true; if (lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT); return; }
-    float v[64];
-    {
-      float t0[32], t1[32];
-      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eh, t0);
-      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eh + 32, t1);
-#pragma unroll
-      for (int i = 0; i < 32; ++i) { v[i] = t0[i]; v[32 + i] = t1[i]; }
-    }
+    float v[32];
+    tmem_ld32(tmem + lane_off + pend_buf * kCqN + 32 * eq, v);
     const int em = 32 * (warp & 3) + lane;                    // == km
-    const int64_t kk = pend_tile * kCqKeys + em;
+    const int kk = (int)pend_tile * kCqKeys + em;             // < 2^31: positions of one row
+    float bm[4];
+    bool bv[4];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int jr = 8 * eh + j;
-      const int r = cur_g * kCqRows + jr;
+    for (int j = 0; j < 4; ++j) {
       float acc = 0.f;
 #pragma unroll
-      for (int h = 0; h < kHIdx; ++h) acc += fmaxf(v[8 * j + h], 0.f) * s_wi[jr][h];
+      for (int h = 0; h < kHIdx; ++h) acc = fmaf(fmaxf(v[8 * j + h], 0.f), wr[j][h], acc);
       float o = acc * pend_ks;
       o = o > 0.f ? o : 0.f;                                  // also maps NaN and -0 to +0
-      const bool valid = kk < s_len[jr];
-      if (valid) a.ws.sigma[(int64_t)r * a.ws.sigma_stride + kk] = o;
+      const bool valid = kk < lenr[j];
+      if (valid) rowp[j][kk] = o;
       smx[j] = fmaxf(smx[j], valid ? pend_ks : 0.f);
       float m = valid ? o : 0.f;
 #pragma unroll
       for (int s = 1; s < BLOCK; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-      if ((em % BLOCK) == 0 && valid) {
-        a.ws.bmax[(int64_t)r * a.ws.nbm + kk / BLOCK] = m;
-        atomicAdd(&a.ws.hist[(int64_t)r * kHistBins + min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)],
-                  1u);
+      bm[j] = m;                                              // the block's maximum, in every lane of it
+      bv[j] = __shfl_sync(0xffffffffu, valid, lane & ~(BLOCK - 1));   // its first position is valid
+    }
+    // lane i of a block writes row i's maximum (BLOCK >= 4), or the block's first lane all four
+    if (BLOCK >= 4) {
+      const int jj = em & (BLOCK - 1);
+      if (jj < 4) {
+        const float m = jj == 0 ? bm[0] : jj == 1 ? bm[1] : jj == 2 ? bm[2] : bm[3];
+        const bool ok = jj == 0 ? bv[0] : jj == 1 ? bv[1] : jj == 2 ? bv[2] : bv[3];
+        if (ok) {
+          float *bp = jj == 0 ? bmaxp[0] : jj == 1 ? bmaxp[1] : jj == 2 ? bmaxp[2] : bmaxp[3];
+          uint32_t *hp = jj == 0 ? histp[0] : jj == 1 ? histp[1] : jj == 2 ? histp[2] : histp[3];
+          bp[(kk - jj) / BLOCK] = m;
+          atomicAdd(&hp[min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+        }
       }
+    } else {
+#pragma unroll
+      for (int j = 0; j < 4; ++j)
+        if ((em % BLOCK) == 0 && bv[j]) {
+          bmaxp[j][kk / BLOCK] = bm[j];
+          atomicAdd(&histp[j][min(__float_as_uint(bm[j]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+        }
     }
   };
 
-  fetch(it0);
+  fetch();
+  advance(g_ft, t_ft);
   for (int64_t it = it0; it < it1; ++it) {
-    const int g = group_of(it);
+    const int g = g_it;
+    const int64_t tile = t_it;
     const int buf = (int)((it - it0) & 1);
-    if (g != cur_g) {
+    const bool newg = g != cur_g;
+    if (newg) {
       // the previous group's last tile completes before its queries are replaced
       if (pend) { epilogue(); pend = false; }
       if (cur_g >= 0) flush_smax();
       if (__syncthreads_or(dead)) break;
-      // queries of group g: (row jr, head h) = MMA column n = 8 jr + h; two threads per pair
-      {
-        const int pair = tid >> 1, half = tid & 1;
-        const int jr = pair >> 3, h = pair & 7;
-        const int r = g * kCqRows + jr;
-        const bool rv = r < a.n;
-        uint32_t wq[16];
-        float mx = 0.f;
-        if (rv) {
-          const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * kHIdx + h) * kDIdx + 32 * half);
+      // queries of group g: (row jr, head h) = MMA column n = 8 jr + h; four threads per pair
+      const int pair = tid >> 2, part = tid & 3;
+      const int jr = pair >> 3, h = pair & 7;
+      const int r = g * kCqRows + jr;
+      const bool rv = r < a.n;
+      uint32_t wq[8];
+      if (rv) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * kHIdx + h) * kDIdx + 16 * part);
+        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+        wq[0] = u0.x; wq[1] = u0.y; wq[2] = u0.z; wq[3] = u0.w;
+        wq[4] = u1.x; wq[5] = u1.y; wq[6] = u1.z; wq[7] = u1.w;
+      } else {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const uint4 u = __ldg(src + i);
-            wq[4 * i] = u.x; wq[4 * i + 1] = u.y; wq[4 * i + 2] = u.z; wq[4 * i + 3] = u.w;
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) wq[i] = 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(wq[i] & 0xFFFFu)), fabsf(bf16_to_f32(wq[i] >> 16))));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        const int c = head_shift(mx);
-        const float sc = pow2f(c);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {                         // dims 32 half + 8 i .. + 7
-          uint32_t o4[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const uint32_t wv = wq[4 * i + e];
-            o4[e] = pack_f16x2(bf16_to_f32(wv & 0xFFFFu) * sc, bf16_to_f32(wv >> 16) * sc);
-          }
-          *reinterpret_cast<uint4 *>(qs + cq_off(pair, 4 * half + i)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
-        }
-        if (half == 0) s_wi[jr][h] = rv ? __ldg(a.w + (int64_t)r * kHIdx + h) * pow2f(-c) : 0.f;
-        if (tid < kCqRows) s_len[tid] = (g * kCqRows + tid < a.n) ? a.len_v[g * kCqRows + tid] : 0;
+        for (int i = 0; i < 8; ++i) wq[i] = 0u;
       }
+      float mx = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        mx = fmaxf(mx, fmaxf(fabsf(bf16_to_f32(wq[i] & 0xFFFFu)), fabsf(bf16_to_f32(wq[i] >> 16))));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+      const int c = head_shift(mx);
+      const float sc = pow2f(c);
+#pragma unroll
+      for (int i = 0; i < 2; ++i) {                           // dims 16 part + 8 i .. + 7
+        uint32_t o4[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const uint32_t wv = wq[4 * i + e];
+          o4[e] = pack_f16x2(bf16_to_f32(wv & 0xFFFFu) * sc, bf16_to_f32(wv >> 16) * sc);
+        }
+        *reinterpret_cast<uint4 *>(qs + cq_off(pair, 2 * part + i)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
+      }
+      if (part == 0) s_wi[jr][h] = rv ? __ldg(a.w + (int64_t)r * kHIdx + h) * pow2f(-c) : 0.f;
+      if (tid < kCqRows) s_len[tid] = (g * kCqRows + tid < a.n) ? a.len_v[g * kCqRows + tid] : 0;
       cur_g = g;
     }
     // ---- this tile's keys, exactly to f16, into its buffer; then the next tile's loads
     {
       uint8_t *kb = s_dyn + kCqK + buf * kCqTileBytes;
-      const uint32_t w8[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {                           // dims 32 dh + 8 i .. + 7
-        const uint32_t lo = w8[2 * i], hi = w8[2 * i + 1];
-        *reinterpret_cast<uint4 *>(kb + cq_off(km, 4 * dh + i)) =
-            make_uint4(e4m3x2_to_f16x2(lo), e4m3x2_to_f16x2(lo >> 16), e4m3x2_to_f16x2(hi),
-                       e4m3x2_to_f16x2(hi >> 16));
-      }
+      *reinterpret_cast<uint4 *>(kb + cq_off(km, 2 * dq)) =
+          make_uint4(e4m3x2_to_f16x2(x0.x), e4m3x2_to_f16x2(x0.x >> 16), e4m3x2_to_f16x2(x0.y),
+                     e4m3x2_to_f16x2(x0.y >> 16));
+      *reinterpret_cast<uint4 *>(kb + cq_off(km, 2 * dq + 1)) =
+          make_uint4(e4m3x2_to_f16x2(x0.z), e4m3x2_to_f16x2(x0.z >> 16), e4m3x2_to_f16x2(x0.w),
+                     e4m3x2_to_f16x2(x0.w >> 16));
     }
     const float cur_ks = xs;
-    if (it + 1 < it1) fetch(it + 1);
+    if (it + 1 < it1) { fetch(); advance(g_ft, t_ft); }
     fence_async_smem();
     tc_fence_before();
     if (__syncthreads_or(dead)) break;
     tc_fence_after();
+    if (newg) {                                               // this thread's rows of the new group
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int jr = 4 * eq + j;
+        lenr[j] = s_len[jr];
+        const int64_t r = (int64_t)g * kCqRows + jr;
+        rowp[j] = a.ws.sigma + r * a.ws.sigma_stride;
+        bmaxp[j] = a.ws.bmax + r * a.ws.nbm;
+        histp[j] = a.ws.hist + r * kHistBins;
+#pragma unroll
+        for (int h = 0; h < kHIdx; ++h) wr[j][h] = s_wi[jr][h];
+      }
+    }
     if (tid == 0) {
       const uint32_t kb_a = ks_a + buf * kCqTileBytes;
 #pragma unroll
@@ -270,9 +306,10 @@ __global__ void __launch_bounds__(kCqThreads, 2) chunk_scores_tc_kernel(const __
     __syncwarp();
     if (pend) epilogue();
     pend = true;
-    pend_tile = it - s_first[g];
+    pend_tile = tile;
     pend_buf = buf;
     pend_ks = cur_ks;
+    advance(g_it, t_it);
   }
   dead = __syncthreads_or(dead);
   if (pend && !dead) epilogue();
@@ -291,7 +328,7 @@ static cudaError_t launch_cq(const CqArgs &a, cudaStream_t st) {
     cudaFuncSetAttribute(chunk_scores_tc_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCqSmemLaunch);
     optin = true;
   }
-  return launch_k(chunk_scores_tc_kernel<BLOCK>, dim3((unsigned)(2 * num_sms())), dim3(kCqThreads), kCqSmemLaunch, st,
+  return launch_k(chunk_scores_tc_kernel<BLOCK>, dim3((unsigned)num_sms()), dim3(kCqThreads), kCqSmemLaunch, st,
                   0, a);
 }
 
