@@ -38,9 +38,9 @@ SCAN_BYTES_PER_POS = 72          # per cached position: 64 FP8 key bytes + 4-byt
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one scan launch, from one ncu
 # capture (profiles/indexer_scan_b32_ctx65536.md), valid only while the scan's sources are
 # the ones captured: the digest covers them, and any change reports the traffic as null.
-SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142715904 + 5656832}
+SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142720256 + 5331968}
 SCAN_NCU_SOURCES = ("sparse_attention_fp4_02_b300/csrc/indexer.cu", "sparse_attention_fp4_02_b300/csrc/common.cuh")
-SCAN_NCU_DIGEST = "6da9b0a5ddb0c672c249d13d6877ca9cf79e23ec3a08d061b04053c38cf8cede"
+SCAN_NCU_DIGEST = "6e1fe76be3c29af4dba078e43ca6062e7a29f4518edbbfd33b946172f3e62a99"
 
 
 def scan_traffic(workload: str):
