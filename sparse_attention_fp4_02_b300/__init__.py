@@ -7,9 +7,10 @@ library has not been built, importing this package raises: there is no CPU
 fallback.
 
 Entry points (same names as the C ABI): ``kv_append_fp4``, ``swa_refill_fp8``,
-``indexer_full_select``, ``indexer_reindex_select``, ``indexer_verify_select``, ``indexer_chunked_select``, ``sparse_attn_decode``,
-plus ``workspace_bytes`` and the ``Cache`` / ``SwaRing`` containers that own
-the device tensors of the layouts the header documents.
+``indexer_full_select``, ``indexer_reindex_select``, ``indexer_reindex_select_static``,
+``indexer_verify_select``, ``indexer_chunked_select``, ``sparse_attn_decode``, plus
+``workspace_bytes`` and the ``Cache`` / ``SwaRing`` containers that own the device
+tensors of the layouts the header documents.
 """
 from __future__ import annotations
 
@@ -79,8 +80,9 @@ _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _
 _t_cscores = _sig("csa2_test_chunk_scores", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P])
 
 EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "swa_refill_fp8", "indexer_full_select",
-            "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select", "indexer_chunked_select", "sparse_attn_decode", "csa2_test_quantize_fp4",
-            "csa2_test_quantize_fp8", "csa2_test_index_scores", "csa2_test_chunk_scores")
+            "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select",
+            "indexer_chunked_select", "sparse_attn_decode", "csa2_test_quantize_fp4", "csa2_test_quantize_fp8",
+            "csa2_test_index_scores", "csa2_test_chunk_scores")
 
 
 class Csa2Error(RuntimeError):
