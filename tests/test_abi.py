@@ -88,3 +88,39 @@ def test_misaligned_cache_rejected_without_a_gpu(lib):
     r = lib.kv_append_fp4(ctypes.byref(desc), None, 0, None, None, None, None, None, ctypes.c_int64(1), None, None,
                           ctypes.c_int64(0), ctypes.byref(err), None)
     assert r == 1          # kv_codes not 16-byte aligned
+
+
+def test_row_mode_workspace_sizes(lib):
+    f = lib.csa2_workspace_bytes
+    out = ctypes.c_size_t(0)
+    args = lambda op, L, blk, nk, k, T: (op, 1, ctypes.c_int64(L), blk, nk, k, ctypes.c_int64(T), 16, 128,
+                                          ctypes.byref(out))
+    # verify rows: sized by rows and pool, independent of the context
+    assert f(*args(4, 0, 8, 2048, 512, 160)) == 0
+    v160 = out.value
+    assert f(*args(4, 0, 8, 2048, 512, 320)) == 0 and out.value > v160
+    assert f(*args(4, 0, 8, 2048, 512, 70000)) == 1        # more than 65,535 rows
+    assert f(*args(4, 0, 8, 16, 32, 5)) == 1               # topk > n_keep_blocks
+    # chunked rows: per-row tables for every row plus one group's selection workspace
+    assert f(*args(5, 262144, 8, 2048, 512, 4096)) == 0
+    c4096 = out.value
+    assert c4096 > 1024 * 262144 * 4                       # the group's stored scores alone
+    assert f(*args(5, 262144, 8, 2048, 512, 1024)) == 0 and out.value < c4096
+    assert f(*args(5, 262144, 8, 2048, 512, (1 << 24) + 1)) == 1
+    assert f(*args(5, 262144, 5, 2048, 512, 16)) == 1      # block not a power of two
+
+
+def test_row_mode_entry_points_reject_bad_arguments_without_a_gpu(lib):
+    z64, zsz = ctypes.c_int64, ctypes.c_size_t
+    assert lib.indexer_verify_select(None, None, None, None, None, z64(5), None, 8, 2048, 512, z64(100), None, None,
+                                     zsz(0), None, None) == 1
+    assert lib.indexer_chunked_select(None, None, None, None, None, z64(5), 8, 2048, 512, z64(100), None, None, None,
+                                      zsz(0), None, None) == 1
+    assert lib.indexer_reindex_select_static(None, None, None, None, 8, 2048, 512, z64(100), None, None, None) == 1
+    assert lib.csa2_test_chunk_scores(None, None, None, None, None, z64(16), z64(100), None, None, None, zsz(0),
+                                      None, None) == 1
+    err = ctypes.c_int32(0)
+    # no ring descriptors, or more sequences than the limit
+    assert lib.swa_refill_fp8(None, 1, 4, None, None, None, z64(1), None, None, z64(1), ctypes.byref(err), None) == 1
+    assert lib.swa_refill_fp8(None, 1, 5000, None, None, None, z64(1), None, None, z64(1), ctypes.byref(err),
+                              None) == 1

@@ -55,3 +55,17 @@ def test_single_rank_is_its_own_maximum():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.aggregate_rate(10, 1, 1000.0) == pytest.approx(10.0)
 
+
+
+def test_launch_counts_per_step():
+    """The gpu_launches claim: append, Full select (clear, scan, [collect,] finalize), three per
+    Reindex (clear, score, select), one attention per layer, and with draft rows three more
+    per indexer layer for the rows' own selection."""
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth.workloads import config, verify_workload
+    assert bench.kernels_per_step(config(1)) == 1 + 3 + 4                  # 8192 blocks: no collect
+    assert bench.kernels_per_step(config(2)) == 1 + 4 + 3 * 4 + 20         # 131072 blocks: collect
+    v = verify_workload()
+    assert v.drafts == 5 and v.ring >= v.window + v.drafts - 1
+    assert bench.kernels_per_step(v) == 1 + 3 + 3 * 5 + 20
