@@ -22,7 +22,12 @@
  *
  * Conventions for every entry point:
  *   - all buffers are caller-owned device memory unless stated otherwise;
- *     the library allocates nothing and keeps no state between calls;
+ *     the library allocates nothing.  Between calls it keeps only (a) a table
+ *     of per-device launch facts (SM count, CTAs per SM of a kernel, the
+ *     opt-in to large dynamic shared memory), filled on a device's first call
+ *     and keyed by device, so that several host threads and several devices
+ *     can call concurrently, and (b) the static scratch array of
+ *     indexer_reindex_select_static (see its Set-up and Sharing notes);
  *   - every call only enqueues work on `stream` (no synchronisation, no
  *     host<->device copy), so calls can be captured into CUDA graphs;
  *   - the return value is a CSA2_STATUS code; arguments are validated on the
@@ -352,6 +357,11 @@ int csa2_test_index_scores(const csa2_cache *cache, const uint16_t *q_idx, const
 int csa2_test_chunk_scores(const csa2_cache *cache, const uint16_t *q_idx, const float *w, const int32_t *q_seq,
                            const int64_t *q_pos, int64_t T, int64_t max_len, float *sigma, double *bound, void *ws,
                            size_t ws_bytes, int32_t *d_err, csa2_stream_t stream);
+
+/* Test: the per-device launch-fact table with an explicit device id and no CUDA call.
+ * Returns the value held for (device, site, key), or stores and returns `value` if there
+ * is none (a negative value is returned without being stored). */
+int csa2_test_device_memo(int device, int site, int64_t key, int value);
 
 #ifdef __cplusplus
 }

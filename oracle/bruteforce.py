@@ -66,3 +66,24 @@ def attend(q, rows, tau):
         out.append([sum(e[j] * rows[j][d] for j in range(len(rows))) / l for d in range(len(qh))])
         lses.append(m + math.log(l))
     return out, lses
+
+
+def e2m1(code: int) -> float:
+    """Value of a 4-bit E2M1 code (sign bit 3, magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6)."""
+    mag = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)[code & 7]
+    return -mag if code & 8 else mag
+
+
+def fp4_row(codes, scales):
+    """One packed FP4 cache row (64 bytes, 8 E4M3 group scales) back to 128 floats."""
+    out = []
+    for j, byte in enumerate(codes):
+        s = e4m3(scales[(2 * j) // 16])
+        out.append(e2m1(byte & 0xF) * s)
+        out.append(e2m1(byte >> 4) * s)
+    return out
+
+
+def fp8_row(codes, scale):
+    """One FP8 row (E4M3 codes and a per-row float scale) back to floats."""
+    return [e4m3(c) * scale for c in codes]

@@ -69,8 +69,33 @@ def layer_inputs(wl: DecodeWorkload, b: int, layer: int, j: int | None = None):
     return q, qi, w
 
 
+def new_token_inputs(wl: DecodeWorkload, b: int, rope=None):
+    """The step's own inputs to the append: bf16 main KV [D][128], indexer key [D][64] and SWA
+    KV of every layer [layers][D][128] of the D = wl.drafts new tokens (positions L-D..L-1),
+    with their rows of the rotation tables."""
+    L = int(wl.lengths[b])
+    cos, sin = rope if rope is not None else synth.rope_table(L)
+    pos = np.arange(L - wl.drafts, L)
+    rows = synth.row_id(b, pos)
+    kv = synth.normals_bf16(wl.seed, synth.Stream.KV, 0, rows, 128,
+                            synth.outlier_channels(wl.seed, synth.Stream.KV_OUTLIER))
+    ik = synth.normals_bf16(wl.seed, synth.Stream.IK, 0, rows, 64)
+    oc = synth.outlier_channels(wl.seed, synth.Stream.SWA_OUTLIER)
+    sw = [synth.normals_bf16(wl.seed, synth.Stream.SWA, l, rows, 128, oc) for l in range(wl.n_layers)]
+    return kv, ik, sw, cos[pos], sin[pos]
+
+
+def append_token(new_inputs):
+    """Quantise-and-append of the step's new tokens (origotech.dev deep dive, subsection "FP4와
+    SWA Bounded Replay"): their cache rows (FP4 main KV, FP8 indexer key) and one FP8 window
+    row per layer."""
+    kv, ik, sw, cos, sin = new_inputs
+    return ap.append_rows(kv, ik, cos, sin), [ap.swa_rows(x, cos, sin) for x in sw]
+
+
 def prepare(wl: DecodeWorkload, b: int, layers=None):
-    """Per-sequence state that exists before the step: cache rows 0..L-1, window rings, layer inputs."""
+    """Per-sequence state that exists before the step: cache rows 0..L-1, window rings, layer
+    inputs, and the new tokens' append inputs ('new')."""
     L = int(wl.lengths[b])
     rope = synth.rope_table(L)
     layers = list(range(wl.n_layers)) if layers is None else list(layers)
@@ -81,6 +106,7 @@ def prepare(wl: DecodeWorkload, b: int, layers=None):
         "rows": ({l: [layer_inputs(wl, b, l, j) for j in range(wl.drafts)] for l in range(max(layers) + 1)}
                  if wl.drafts > 1 else None),
         "layers": layers,
+        "new": new_token_inputs(wl, b, rope),
     }
 
 

@@ -78,11 +78,12 @@ _t_fp4 = _sig("csa2_test_quantize_fp4", [_P, _I64, _P, _P, _P])
 _t_fp8 = _sig("csa2_test_quantize_fp8", [_P, _I64, _I32, _P, _P, _P])
 _t_scores = _sig("csa2_test_index_scores", [_P, _P, _P, _I64, _P, _P, _P, _SZ, _P, _P])
 _t_cscores = _sig("csa2_test_chunk_scores", [_P, _P, _P, _P, _P, _I64, _I64, _P, _P, _P, _SZ, _P, _P])
+_t_memo = _sig("csa2_test_device_memo", [_I32, _I32, _I64, _I32])
 
 EXPORTED = ("csa2_status_string", "csa2_workspace_bytes", "kv_append_fp4", "swa_refill_fp8", "indexer_full_select",
             "indexer_reindex_select", "indexer_reindex_select_static", "indexer_verify_select",
             "indexer_chunked_select", "sparse_attn_decode", "csa2_test_quantize_fp4", "csa2_test_quantize_fp8",
-            "csa2_test_index_scores", "csa2_test_chunk_scores")
+            "csa2_test_index_scores", "csa2_test_chunk_scores", "csa2_test_device_memo")
 
 
 class Csa2Error(RuntimeError):

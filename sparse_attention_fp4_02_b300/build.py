@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libcsa2.so")
-SOURCES = ["append.cu", "indexer.cu", "indexer_tc.cu", "attention.cu", "attention_tc.cu", "api.cu"]
+SOURCES = ["append.cu", "indexer.cu", "indexer_tc.cu", "attention.cu", "attention_tc.cu", "api.cu", "device_state.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include"), "-I", CSRC]

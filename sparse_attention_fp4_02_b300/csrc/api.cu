@@ -14,19 +14,19 @@ bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
 int cuda_status(cudaError_t e) { return e == cudaSuccess ? CSA2_OK : CSA2_ERR_CUDA; }
 
-// compute capability 10.3 check, cached per device
+// compute capability 10.3 check, memoised per device
 int device_ok() {
-  static int cached[64] = {0};   // 0 unknown, 1 ok, 2 unsupported
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return CSA2_ERR_CUDA;
-  if (dev < 0 || dev >= 64) return CSA2_ERR_UNSUPPORTED;
-  if (cached[dev] == 0) {
+  const int ok = device_memo(kSiteDeviceOk, 0, [dev] {
     int major = 0, minor = 0;
-    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
-    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
-    cached[dev] = (major == 10 && minor == 3) ? 1 : 2;
-  }
-  return cached[dev] == 1 ? CSA2_OK : CSA2_ERR_UNSUPPORTED;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+      return -1;
+    return (major == 10 && minor == 3) ? 1 : 0;
+  });
+  if (ok < 0) return CSA2_ERR_CUDA;
+  return ok == 1 ? CSA2_OK : CSA2_ERR_UNSUPPORTED;
 }
 
 bool cache_ok(const csa2_cache *c) {
@@ -240,7 +240,8 @@ namespace {
 // for cudaGetSymbolAddress, never a device address.
 __device__ __align__(256) unsigned char g_reindex_scratch[CSA2_STATIC_SCRATCH_BYTES];
 
-// The array's device address on the current device, resolved once per device.
+// The array's device address on the current device, resolved once per device (with that
+// device current) and kept beside the library's other per-device facts.
 int static_scratch(void **out) {
   static std::mutex mu;
   static void *addr[64] = {};

@@ -478,11 +478,7 @@ cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const u
   if (T == 0) return cudaSuccess;
   if (attn_tc_eligible(T, H))
     return launch_attn_chunked_tc(c, swa, q, H, T, q_seq, q_pos, topk_idx, topk, window, tau, out, lse, d_err, st);
-  static bool optin = false;
-  if (!optin) {
-    cudaFuncSetAttribute(attn_decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)attn_smem(kMaxSplit));
-    optin = true;
-  }
+  opt_in_smem((const void *)attn_decode_kernel, attn_smem(kMaxSplit), kSiteAttnOptin, 0);
   AttnArgs a;
   a.c = c; a.swa = swa; a.q = q; a.H = H; a.T = T; a.q_seq = q_seq; a.q_pos = q_pos;
   a.topk_idx = topk_idx; a.topk = topk; a.window = window; a.tau = tau; a.out = out; a.lse = lse;

@@ -406,11 +406,7 @@ bool attn_tc_eligible(int64_t T, int H) { return H >= 16 && H <= kTcMaxH && (H %
 cudaError_t launch_attn_chunked_tc(const csa2_cache &c, const csa2_swa &swa, const uint16_t *q, int H, int64_t T,
                                    const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx, int topk,
                                    int window, float tau, float *out, float *lse, int32_t *d_err, cudaStream_t st) {
-  static bool optin = false;
-  if (!optin) {
-    cudaFuncSetAttribute(attn_chunked_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmemLaunch);
-    optin = true;
-  }
+  opt_in_smem((const void *)attn_chunked_tc_kernel, kTcSmemLaunch, kSiteAttnTcOptin, 0);
   TcArgs a;
   a.c = c; a.swa = swa; a.q = q; a.H = H; a.T = T; a.q_seq = q_seq; a.q_pos = q_pos;
   a.topk_idx = topk_idx; a.topk = topk; a.window = window; a.tau = tau; a.out = out; a.lse = lse; a.d_err = d_err;

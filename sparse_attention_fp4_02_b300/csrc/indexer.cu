@@ -17,8 +17,10 @@
 // f16 conversion of the queries) and r = 2^-19 (epilogue rounding).  For a top-k by
 // value, with theta~ the k-th largest approximate value, an item is certainly in if
 // sigma~ > ((1+r) theta~ + 2E)/(1-r), certainly out if sigma~ < ((1-r) theta~ - 2E)/(1+r),
-// and otherwise rescored in float64 (exact products, float64 sums) before the final
-// choice by (score desc, id asc).
+// and otherwise rescored exactly before the final choice by (score desc, id asc): each
+// head's dot product as a sum of exact integer products in 64-bit fixed point, then ReLU,
+// head weights and the key scale in double-float (float pairs with error-free TwoSum and
+// TwoProduct, 48 significant bits).
 #include <cfloat>
 #include <algorithm>
 #include <climits>
@@ -1500,17 +1502,6 @@ IndexerWs indexer_ws_carve(void *ws, int32_t B, int64_t max_len, int32_t block, 
   return w;
 }
 
-static int g_num_sms = 0;
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 148;
-  }
-  return g_num_sms;
-}
-
 static size_t scan_smem_bytes(int B, bool priv) {
   return kScanSmem + (priv ? (size_t)kHistBins * 4 : 0) + (size_t)(2 * B + 1) * 8 + (size_t)B * 4;
 }
@@ -1523,19 +1514,17 @@ static bool scan_private_hist(int64_t max_len) { return max_len >= 262144; }
 // persistent scan grid: every resident CTA slot of the GPU, capped by the work
 template <int BLOCK, bool PRIV>
 static int scan_grid_size(int B, int64_t max_len) {
-  static int per_sm = 0, for_b = -1;
-  if (for_b != B) {
-    const size_t smem = scan_smem_bytes(B, PRIV);
-    cudaFuncSetAttribute(scan_kernel<BLOCK, false, PRIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)scan_smem_bytes(CSA2_MAX_B, PRIV));
-    cudaFuncSetAttribute(scan_kernel<BLOCK, true, PRIV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)scan_smem_bytes(CSA2_MAX_B, PRIV));
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, scan_kernel<BLOCK, false, PRIV>, kScanWarps * 32,
-                                                      smem) != cudaSuccess ||
-        per_sm < 1)
-      per_sm = 1;
-    for_b = B;
-  }
+  opt_in_smem((const void *)scan_kernel<BLOCK, false, PRIV>, scan_smem_bytes(CSA2_MAX_B, PRIV), kSiteScanOptin,
+              BLOCK * 4 + PRIV * 2 + 0);
+  opt_in_smem((const void *)scan_kernel<BLOCK, true, PRIV>, scan_smem_bytes(CSA2_MAX_B, PRIV), kSiteScanOptin,
+              BLOCK * 4 + PRIV * 2 + 1);
+  const int per_sm = device_memo(kSiteScanOccupancy, ((int64_t)B << 8) | (BLOCK << 1) | (PRIV ? 1 : 0), [B] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, scan_kernel<BLOCK, false, PRIV>, kScanWarps * 32,
+                                                      scan_smem_bytes(B, PRIV)) != cudaSuccess || n < 1)
+      return 1;
+    return n;
+  });
   const int64_t stages_ub = (int64_t)B * ((max_len + 31) / 32);
   const int64_t g = std::min<int64_t>((stages_ub + kScanWarps - 1) / kScanWarps, (int64_t)num_sms() * per_sm);
   return (int)std::max<int64_t>(g, 1);
@@ -1562,30 +1551,21 @@ constexpr size_t kSelectSmemStaged = kSelectSmemBase + (size_t)kStageItems * 4;
 
 template <int BLOCK>
 static void select_smem_optin() {
-  static bool done = false;
-  if (!done) {
-    cudaFuncSetAttribute(finalize_blocks_kernel<BLOCK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kFinalizeSmemDirect);
-    cudaFuncSetAttribute(finalize_blocks_kernel<BLOCK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kFinalizeSmemCand);
-    cudaFuncSetAttribute(select_positions_kernel<BLOCK, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSelectSmemStaged);
-    cudaFuncSetAttribute(select_positions_kernel<BLOCK, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         (int)kSelectSmemBase);
-    done = true;
-  }
+  opt_in_smem((const void *)finalize_blocks_kernel<BLOCK, true>, kFinalizeSmemDirect, kSiteSelectOptin, BLOCK * 4 + 0);
+  opt_in_smem((const void *)finalize_blocks_kernel<BLOCK, false>, kFinalizeSmemCand, kSiteSelectOptin, BLOCK * 4 + 1);
+  opt_in_smem((const void *)select_positions_kernel<BLOCK, true>, kSelectSmemStaged, kSiteSelectOptin, BLOCK * 4 + 2);
+  opt_in_smem((const void *)select_positions_kernel<BLOCK, false>, kSelectSmemBase, kSiteSelectOptin, BLOCK * 4 + 3);
 }
 
 // CTAs per row of the position scoring: enough resident warps on every SM, at most 32 per row.
 template <int BLOCK>
 static int positions_grid(int rows) {
-  static int resident = 0;
-  if (resident == 0) {
+  const int resident = device_memo(kSitePositionsResident, BLOCK, [] {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, score_positions_kernel<BLOCK>, 256, 0) != cudaSuccess || n < 1)
       n = 2;
-    resident = std::min(n, 4);
-  }
+    return std::min(n, 4);
+  });
   return std::max(1, std::min(32, (int)((int64_t)num_sms() * resident / std::max(rows, 1))));
 }
 

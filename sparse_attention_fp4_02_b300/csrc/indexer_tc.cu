@@ -323,11 +323,7 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
 
 template <int BLOCK>
 static cudaError_t launch_cq(const CqArgs &a, cudaStream_t st) {
-  static bool optin = false;
-  if (!optin) {
-    cudaFuncSetAttribute(chunk_scores_tc_kernel<BLOCK>, cudaFuncAttributeMaxDynamicSharedMemorySize, kCqSmemLaunch);
-    optin = true;
-  }
+  opt_in_smem((const void *)chunk_scores_tc_kernel<BLOCK>, kCqSmemLaunch, kSiteChunkScoresOptin, BLOCK);
   return launch_k(chunk_scores_tc_kernel<BLOCK>, dim3((unsigned)num_sms()), dim3(kCqThreads), kCqSmemLaunch, st,
                   0, a);
 }

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <functional>
 #include <cuda_runtime.h>
 
 #include "csa2.h"
@@ -90,6 +91,24 @@ cudaError_t launch_attn_chunked_tc(const csa2_cache &c, const csa2_swa &swa, con
                                    const int32_t *q_seq, const int64_t *q_pos, const int32_t *topk_idx, int topk,
                                    int window, float tau, float *out, float *lse, int32_t *d_err, cudaStream_t st);
 
+// ---- per-device launch facts (device_state.cu) ----
+enum MemoSite {
+  kSiteDeviceOk = 1,
+  kSiteNumSms,
+  kSiteScanOccupancy,
+  kSiteScanOptin,
+  kSiteSelectOptin,
+  kSitePositionsResident,
+  kSiteAttnOptin,
+  kSiteAttnTcOptin,
+  kSiteChunkScoresOptin,
+};
+// The value memoised for (device, site, key); make() computes it on first use (a negative
+// result is not kept).  device_memo uses the current device.
+int memo_lookup(int device, int site, int64_t key, const std::function<int()> &make);
+int device_memo(int site, int64_t key, const std::function<int()> &make);
+// Opt `kernel` in to `bytes` of dynamic shared memory on the current device, once.
+int opt_in_smem(const void *kernel, size_t bytes, int site, int64_t key);
 int num_sms();
 
 }  // namespace csa2

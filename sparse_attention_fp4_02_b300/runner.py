@@ -159,25 +159,53 @@ class DecodeRunner:
         torch.cuda.synchronize()
 
     # ------------------------------------------------------------------ the step
-    def step(self, prof=None):
-        """One decode (or draft-verification) step through every layer of the schedule."""
+    def step(self, prof=None, mark=None):
+        """One decode (or draft-verification) step through every layer of the schedule.
+
+        ``mark``, if given, is called with the entry point's name after each call (the benchmark
+        records a timing event there for its per-call breakdown)."""
         wl = self.wl
+        mark = mark or (lambda name: None)
         kv_append_fp4(self.cache, self.swa, self.kv_new, self.ik_new, self.swa_new, self.rope_cos, self.rope_sin,
                       self.seq_id, self.pos, self.d_err)
+        mark("kv_append_fp4")
         for l, mode in enumerate(wl.schedule):
             if mode == FULL:
                 indexer_full_select(self.cache, self.qidx_last[l], self.w_last[l], wl.block, wl.n_keep, wl.topk,
                                     self.max_len, self.pool, self.topk_full[l], self.ws_idx, self.d_err, prof=prof)
+                mark("indexer_full_select")
             if self.D > 1 and mode in (FULL, REINDEX):
                 indexer_verify_select(self.cache, self.qidx[l], self.w[l], self.seq_id, self.pos, self.pool,
                                       wl.block, wl.n_keep, wl.topk, self.max_len, self.topk[l], self.ws_ver,
                                       self.d_err)
+                mark("indexer_verify_select")
             elif mode == REINDEX:
                 indexer_reindex_select(self.cache, self.qidx[l], self.w[l], self.pool, wl.block, wl.n_keep, wl.topk,
                                        self.max_len, self.topk[l], self.ws_idx, self.d_err)
+                mark("indexer_reindex_select")
             sparse_attn_decode(self.cache, self.swa[l], self.q[l], self.seq_id, self.pos, self.layer_topk(l),
                                wl.window, self.tau, self.out[l], self.lse[l], self.ws_attn, self.d_err)
+            mark("sparse_attn_decode")
 
+    def step_bytes(self) -> dict:
+        """Algorithmic bytes of one step by part: the unique bytes the method must read and write
+        (the scan's 68 B per cached position, a Reindex layer's 68 B per pool position, an
+        attention row's gathered FP4 rows, window rows, indices, queries and outputs, the
+        append's inputs and cache rows); implementation scratch is not counted."""
+        wl, L = self.wl, self.lengths
+        n_re = sum(1 for m in wl.schedule if m == REINDEX)
+        rows_per_seq = self.D
+        attn_row = (np.minimum(L, wl.topk) * 72 + np.minimum(L, wl.window) * 132 + 4 * wl.topk
+                    + 2 * wl.H * 128 + 4 * wl.H * 128 + 4 * wl.H)
+        layers = wl.n_layers
+        tok_read = 2 * 128 + 2 * 64 + layers * 2 * 128 + 2 * 32 * 4
+        tok_write = 72 + 68 + layers * 132
+        return {
+            "scan": int(68 * L.sum()),
+            "reindex": int(68 * np.minimum(L, wl.n_keep * wl.block).sum() * n_re * rows_per_seq),
+            "attention": int(attn_row.sum() * layers * rows_per_seq),
+            "append": int((tok_read + tok_write) * self.T),
+        }
     def check_device_errors(self):
         v = int(self.d_err.item())
         if v:
@@ -280,9 +308,16 @@ class ChunkedRunner:
         return 4.0 * wl.n_query * wl.H * (wl.topk + wl.window) * 128
 
     def bytes(self) -> int:
-        """Algorithmic bytes of one call: gathered FP4 rows, FP8 window rows, indices, q, o."""
+        """Algorithmic bytes of one call: the unique bytes it must move, i.e. every distinct
+        gathered FP4 row (72 B) and window row (132 B) once, the index lists, the bf16 queries
+        and the float32 outputs and lse (rows shared by several queries are counted once)."""
         wl = self.wl
-        return wl.n_query * (wl.topk * 72 + wl.window * 132 + 4 * wl.topk + 2 * wl.H * 128 + 4 * wl.H * 128)
+        idx = self.topk.cpu().numpy()
+        uniq_rows = np.unique(idx[idx >= 0]).shape[0]
+        q_pos = self.q_pos.cpu().numpy()              # consecutive positions: one run of window rows
+        uniq_win = int(q_pos.max() - max(0, q_pos.min() - wl.window + 1) + 1)
+        T, H = wl.n_query, wl.H
+        return int(uniq_rows * 72 + uniq_win * 132 + T * wl.topk * 4 + T * H * 128 * 2 + T * H * 128 * 4 + T * H * 4)
 
     def check_device_errors(self):
         v = int(self.d_err.item())

@@ -124,3 +124,28 @@ def test_row_mode_entry_points_reject_bad_arguments_without_a_gpu(lib):
     assert lib.swa_refill_fp8(None, 1, 4, None, None, None, z64(1), None, None, z64(1), ctypes.byref(err), None) == 1
     assert lib.swa_refill_fp8(None, 1, 5000, None, None, None, z64(1), None, None, z64(1), ctypes.byref(err),
                               None) == 1
+
+
+def test_device_memo_keeps_each_devices_own_values(lib):
+    """The per-device launch-fact table: values are kept per (device, site, key), the first
+    stored value wins, a negative (failed) value is not kept, and concurrent first calls from
+    many host threads agree on one value."""
+    import threading
+    f = lib.csa2_test_device_memo
+    f.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int]
+    f.restype = ctypes.c_int
+    site = 1000                                   # a site no kernel uses
+    assert f(0, site, 7, 148) == 148
+    assert f(1, site, 7, 132) == 132             # another device keeps its own value
+    assert f(0, site, 7, 999) == 148 and f(1, site, 7, 999) == 132
+    assert f(0, site, 8, 3) == 3                 # another key on the same device
+    assert f(5, site, 1, -1) == -1 and f(5, site, 1, 4) == 4      # a failure is retried
+    got = []
+    def worker(v):
+        got.append(f(9, site, 42, v))
+    ts = [threading.Thread(target=worker, args=(v,)) for v in range(1, 33)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert len(set(got)) == 1 and f(9, site, 42, 0) == got[0]
