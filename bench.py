@@ -389,11 +389,11 @@ def oracle_step(wl, states, i):
     pipeline.step(wl, b, states[b])
 
 
-def cpu_baseline(cfg: int, budget_s: float = 10.0):
-    """The oracle as it stands on this host: whole decode steps (append included) of a sample
-    of sequences, timed single-threaded and with one worker thread per host core."""
+def cpu_worker(cfg: int, budget_s: float):
+    """Runs in a child process whose BLAS libraries were started with one thread: times the
+    oracle's whole decode steps single-threaded, then with one worker thread per host core;
+    prints one JSON object."""
     from concurrent.futures import ThreadPoolExecutor
-    from threadpoolctl import threadpool_limits
     from oracle import pipeline
     from synth.workloads import config
 
@@ -401,25 +401,40 @@ def cpu_baseline(cfg: int, budget_s: float = 10.0):
     n_prep = max(1, min(wl.B, 4))
     states = [pipeline.prepare(wl, b) for b in range(n_prep)]
     cores = host_cores()
-    with threadpool_limits(1):
-        n, t0 = 0, time.perf_counter()
-        while n < n_prep or time.perf_counter() - t0 < budget_s / 2:
-            oracle_step(wl, states, n)
-            n += 1
-        single_s = time.perf_counter() - t0
-        single = n / single_s
-        per = max(1, math.ceil(single * budget_s / 2))          # steps per worker (~budget/2 at full scaling)
-        with ThreadPoolExecutor(cores) as ex:
-            t0 = time.perf_counter()
-            list(ex.map(lambda w: [oracle_step(wl, states, w + j * cores) for j in range(per)], range(cores)))
-            multi_s = time.perf_counter() - t0
+    n, t0 = 0, time.perf_counter()
+    while n < n_prep or time.perf_counter() - t0 < budget_s / 2:
+        oracle_step(wl, states, n)
+        n += 1
+    single_s = time.perf_counter() - t0
+    single = n / single_s
+    per = max(1, math.ceil(single * budget_s / 2))          # steps per worker (~budget/2 at full scaling)
+    with ThreadPoolExecutor(cores) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(lambda w: [oracle_step(wl, states, w + j * cores) for j in range(per)], range(cores)))
+        multi_s = time.perf_counter() - t0
     multi = cores * per / multi_s
-    return {"value": multi, "unit": "query-steps/s", "cores": cores, "kind": "oracle",
-            "single_thread": {"value": single, "cores": 1, "steps": n, "seconds": round(single_s, 2)},
-            "all_cores": {"value": multi, "cores": cores, "steps": cores * per, "seconds": round(multi_s, 2)},
-            "sample": f"whole decode steps (append + every layer) of {n_prep} of the {wl.B} sequences of {wl.name}, "
-                      f"cycled; single-threaded ({n} steps, {single_s:.1f} s) and {cores} worker threads with one "
-                      f"BLAS thread each ({cores * per} steps, {multi_s:.1f} s); cache preparation excluded"}
+    print(json.dumps({"value": multi, "unit": "query-steps/s", "cores": cores, "kind": "oracle",
+                      "single_thread": {"value": single, "cores": 1, "steps": n, "seconds": round(single_s, 2)},
+                      "all_cores": {"value": multi, "cores": cores, "steps": cores * per,
+                                    "seconds": round(multi_s, 2)},
+                      "sample": f"whole decode steps (append + every layer) of {n_prep} of the {wl.B} sequences of "
+                                f"{wl.name}, cycled; single-threaded ({n} steps, {single_s:.1f} s) and {cores} "
+                                f"worker threads with one BLAS thread each ({cores * per} steps, {multi_s:.1f} s); "
+                                f"cache preparation excluded"}), flush=True)
+
+
+def cpu_baseline(cfg: int, budget_s: float = 10.0):
+    """The oracle as it stands on this host's cores, in a child process (one BLAS thread per
+    worker thread, set before its libraries start)."""
+    env = dict(os.environ)
+    for var in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+        env[var] = "1"
+    env["CUDA_VISIBLE_DEVICES"] = ""
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--cpu-worker", "--config", str(cfg),
+                        "--cpu-budget", str(budget_s)], capture_output=True, text=True, env=env, cwd=ROOT)
+    if r.returncode != 0:
+        return {"value": None, "unit": "query-steps/s", "kind": "oracle", "error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
 
 
 def workload_line(res, peak):
@@ -549,7 +564,12 @@ def main():
     ap.add_argument("--only-headline", action="store_true",
                     help="time only the --config workload (skip config 0, 1M, ragged, verify, chunked)")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-worker", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.cpu_worker:
+        cpu_worker(args.config, args.cpu_budget)
+        return
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":

@@ -1,4 +1,5 @@
 // C ABI of the CSA2 library: host-side validation, workspace sizing, dispatch.
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -35,7 +36,7 @@ bool cache_ok(const csa2_cache *c) {
   if (!aligned(c->kv_codes, 16) || !aligned(c->kv_scales, 16) || !aligned(c->ik_codes, 16) ||
       !aligned(c->ik_scale, 16) || !aligned(c->seq_base, 8) || !aligned(c->seq_len, 4))
     return false;
-  return c->B >= 1 && c->B <= CSA2_MAX_B && c->T_cap >= 1;
+  return c->B >= 1 && c->B <= CSA2_MAX_B && c->T_cap >= 1 && c->T_cap <= (int64_t)INT32_MAX;
 }
 
 bool block_ok(int32_t block) { return block == 1 || block == 2 || block == 4 || block == 8 || block == 16; }

@@ -465,9 +465,12 @@ size_t attn_ws_bytes(int64_t, int32_t, int32_t, int32_t) { return 0; }
 #ifndef CSA2_ATTN_CTAS_PER_SM
 #define CSA2_ATTN_CTAS_PER_SM 1
 #endif
+#ifndef CSA2_ATTN_MAX_SPLIT
+#define CSA2_ATTN_MAX_SPLIT kMaxSplit
+#endif
 static int attn_split(int64_t rows) {
   int split = 1;
-  while (split < kMaxSplit && rows * split * 2 <= CSA2_ATTN_CTAS_PER_SM * (int64_t)num_sms()) split *= 2;
+  while (split < CSA2_ATTN_MAX_SPLIT && rows * split * 2 <= CSA2_ATTN_CTAS_PER_SM * (int64_t)num_sms()) split *= 2;
   return split;
 }
 

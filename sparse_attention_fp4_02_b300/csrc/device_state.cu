@@ -11,6 +11,7 @@
 #include <mutex>
 #include <tuple>
 
+
 #include "launch.h"
 
 namespace csa2 {

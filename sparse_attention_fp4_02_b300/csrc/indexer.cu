@@ -27,6 +27,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "tcgen05.cuh"
 
 namespace csa2 {
 
@@ -447,14 +448,17 @@ __device__ __forceinline__ SelUnit sel_unit(const IdxArgs &a, int r) {
 
 // ------------------------------------------------------------------ scan
 
+// One CTA of 16 warps per SM: measured on B300, co-resident CTAs of the same kernel progress
+// unevenly (the last-started CTA of each SM finished ~3 us after the first at 64K context),
+// which a single CTA per SM avoids.
 #ifndef CSA2_SCAN_WARPS
-#define CSA2_SCAN_WARPS 8
+#define CSA2_SCAN_WARPS 16
 #endif
 #ifndef CSA2_SCAN_STAGES
 #define CSA2_SCAN_STAGES 4
 #endif
 #ifndef CSA2_SCAN_CTAS
-#define CSA2_SCAN_CTAS 3
+#define CSA2_SCAN_CTAS 1
 #endif
 constexpr int kScanWarps = CSA2_SCAN_WARPS;
 constexpr int kScanStages = CSA2_SCAN_STAGES;
@@ -528,18 +532,28 @@ __device__ __forceinline__ void emit_stage(float o, int lane, int blk0, int rows
   }
 }
 
-// Each warp streams a contiguous range of 32-row stages through its own cp.async ring in
-// shared memory (kScanStages stages), so loads in flight hold no registers.  Stages never
-// straddle sequences: sequence b has ceil(len_b / 32) of them and the warps split the
-// concatenated list evenly.  Stage layout: 32 rows x 64 key bytes, then 32 scales stored
-// so that lane quad g finds rows g, g+8, g+16, g+24 in one 16-byte word.
+// Each warp streams a contiguous range of 32-row stages through its own ring in shared
+// memory (kScanStages stages), so loads in flight hold no registers: a stage's key rows
+// arrive by one TMA bulk copy (issued by lane 0, completing the slot's mbarrier by byte
+// count), its scales by one 4-byte cp.async per lane.  Stages never straddle sequences:
+// sequence b has ceil(len_b / 32) of them and the warps split the concatenated list evenly.
+// Stage layout: 32 rows x 64 key bytes, then 32 scales stored so that lane quad g finds
+// rows g, g+8, g+16, g+24 in one 16-byte word.  Rows past the sequence's end get scale 0
+// (their keys are whatever follows in the cache, or stale), so they score 0.
 template <int BLOCK, bool SIGMA, bool PRIV>
-__global__ void __launch_bounds__(kScanWarps * 32, PRIV ? 2 : CSA2_SCAN_CTAS)
+__global__ void __launch_bounds__(kScanWarps * 32, CSA2_SCAN_CTAS)
     scan_kernel(const __grid_constant__ IdxArgs a) {
   pdl_enter();
   extern __shared__ __align__(16) uint8_t s_dyn[];
+  __shared__ __align__(8) uint64_t s_full[kScanWarps][kScanStages];     // key rows of each ring slot
   static_assert((kScanStages & (kScanStages - 1)) == 0, "ring length must be a power of two");
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (lane == 0) {
+    for (int i = 0; i < kScanStages; ++i)
+      asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(smem_addr(&s_full[warp][i])));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  __syncwarp();
   const int B = a.c.B;
   uint32_t *s_hist = reinterpret_cast<uint32_t *>(s_dyn + kScanSmem);   // PRIV: [kHistBins] home sequence's counts
   int64_t *s_first = reinterpret_cast<int64_t *>(s_hist + (PRIV ? kHistBins : 0));   // [B + 1] first stage of each sequence
@@ -588,39 +602,33 @@ __global__ void __launch_bounds__(kScanWarps * 32, PRIV ? 2 : CSA2_SCAN_CTAS)
   const uint32_t ring_s = (uint32_t)__cvta_generic_to_shared(ring);
   const uint32_t sc_dst = kStageRows * kDIdx + 4 * ((lane & 7) * 4 + (lane >> 3));
 
-  // producer cursor: sequence, stage within it, its stage count and length, source rows
+  // producer cursor: sequence, stage within it, its stage count and length, first row
   int pb = b0, ps = (int)(g_begin - s_first[b0]);
   int pn = (int)(s_first[b0 + 1] - s_first[b0]), plen = s_len[b0];
-  const uint8_t *psrc = a.c.ik_codes + (s_base[b0] + 32 * (int64_t)ps) * kDIdx + 16 * t;
-  const float *pscale = a.c.ik_scale + s_base[b0] + 32 * (int64_t)ps + lane;
-  // issue the gathers of this warp's next stage into ring slot k
+  int64_t prow = s_base[b0] + 32 * (int64_t)ps;
+  // issue the loads of this warp's next stage into ring slot k
   auto issue_stage = [&](int k) {
     if (ps == pn) {                                              // next sequence with stages
       do { ++pb; } while (s_first[pb + 1] == s_first[pb]);
       ps = 0;
       pn = (int)(s_first[pb + 1] - s_first[pb]);
       plen = s_len[pb];
-      psrc = a.c.ik_codes + s_base[pb] * kDIdx + 16 * t;
-      pscale = a.c.ik_scale + s_base[pb] + lane;
+      prow = s_base[pb];
     }
-    const uint32_t dst = ring_s + (uint32_t)(k & (kScanStages - 1)) * kStageBytes;
+    const int slot = k & (kScanStages - 1);
+    const uint32_t dst = ring_s + (uint32_t)slot * kStageBytes;
     const int rows = min(32, plen - 32 * ps);
-    if (rows == 32) {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) cp_async16(dst + (g + 8 * q) * kDIdx + 16 * t, psrc + (g + 8 * q) * kDIdx, true);
-      cp_async4(dst + sc_dst, pscale, true);
-    } else {
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const bool v = g + 8 * q < rows;
-        cp_async16(dst + (g + 8 * q) * kDIdx + 16 * t, v ? psrc + (g + 8 * q) * kDIdx : a.c.ik_codes, v);
-      }
-      cp_async4(dst + sc_dst, lane < rows ? pscale : a.c.ik_scale, lane < rows);
+    if (lane == 0) {                                             // key rows that exist in the cache
+      const int64_t avail = a.c.T_cap - prow;
+      const uint32_t bytes = (uint32_t)(avail < kStageRows ? avail : kStageRows) * kDIdx;
+      fence_async_smem();                                        // the slot's last reads precede the copy
+      mbar_expect_tx_u32(smem_addr(&s_full[warp][slot]), bytes);
+      bulk_copy_g2s(dst, a.c.ik_codes + prow * kDIdx, bytes, smem_addr(&s_full[warp][slot]));
     }
+    cp_async4(dst + sc_dst, lane < rows ? a.c.ik_scale + prow + lane : a.c.ik_scale, lane < rows);
     cp_async_commit();
     ++ps;
-    psrc += kStageRows * kDIdx;
-    pscale += kStageRows;
+    prow += kStageRows;
   };
   const int pre = min(kScanStages - 1, nst);
   for (int s = 0; s < pre; ++s) issue_stage(s);
@@ -636,6 +644,8 @@ __global__ void __launch_bounds__(kScanWarps * 32, PRIV ? 2 : CSA2_SCAN_CTAS)
   uint32_t *hist = a.ws.hist + (int64_t)cb * kHistBins;
   bool home = cb == home_b;
   auto consume = [&](int k) {
+    const bool landed = mbar_wait(smem_addr(&s_full[warp][k & (kScanStages - 1)]), (k / kScanStages) & 1);
+    if (!landed && lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT);
     cp_async_wait<kScanStages - 1>();
     __syncwarp();
     if (cs == cn) {                                              // a new sequence: its queries and weights
