@@ -138,15 +138,35 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     const int ti = tw0 + s, j = ti * kTileRows + r;
     idx_pre[s] = (ti < tw1_max && ti < a.tiles_sel && j < a.topk) ? __ldg(idx_row + j) : -1;
   }
+  // the row's sequence, and its base and length: for up to 128 sequences every lane also
+  // loads four table entries at once, so the entry of the row's sequence comes by shuffle
+  // instead of a second dependent load
   const int b = a.q_seq[t];
   const int64_t p = a.q_pos[t];
+  int64_t tb[4];
+  int32_t tl[4];
+  const bool small_table = a.c.B <= 128;
+  if (small_table) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int e = lane + 32 * j;
+      tb[j] = e < a.c.B ? a.c.seq_base[e] : 0;
+      tl[j] = e < a.c.B ? a.c.seq_len[e] : 0;
+    }
+  }
   bool ok = b >= 0 && b < a.c.B;
   int64_t base = 0, len = 0;
-  if (ok) {
+  if (small_table) {
+    const int bs = ok ? b : 0, j = bs >> 5;
+    const int64_t bj = j == 0 ? tb[0] : j == 1 ? tb[1] : j == 2 ? tb[2] : tb[3];
+    const int32_t lj = j == 0 ? tl[0] : j == 1 ? tl[1] : j == 2 ? tl[2] : tl[3];
+    base = __shfl_sync(0xffffffffu, bj, bs & 31);
+    len = __shfl_sync(0xffffffffu, lj, bs & 31);
+  } else if (ok) {
     base = a.c.seq_base[b];
     len = a.c.seq_len[b];
-    ok = p >= 0 && p < len && base >= 0 && base + len <= a.c.T_cap;
   }
+  if (ok) ok = p >= 0 && p < len && base >= 0 && base + len <= a.c.T_cap;
   if (!ok && hg == 0 && crank == 0 && tid == 0)
     set_err(a.d_err, (b < 0 || b >= a.c.B) ? CSA2_DEVERR_SEQ : CSA2_DEVERR_POS);
 
