@@ -4,21 +4,19 @@
 // 압축하다", section "CSA2와 어텐션 재설계"; origotech.dev deep dive, subsection "Compressed
 // Sparse Attention 2(CSA2)"): one softmax over a row's selected FP4 rows plus its FP8
 // window, V = K.  With many query rows and 64 heads every gathered key row is shared by all
-// heads of its query row, so the two products are dense contractions:
-//   S^T = K Q^T      (M = 128 key rows of a chunk, N = H heads, K = 128 dims)
-//   O^T += V^T P^T   (M = 128 dims,               N = H heads, K = 128 key rows)
-//   l   += 1 P^T     (the row sums, from the same f16 P, on the tensor cores too)
+// heads of its query row, so the two products are dense contractions, per chunk of 128 keys:
+//   S = Q K^T      (M = 64 heads, N = 128 keys, K = 128 dims)
+//   O += P V       (M = 64 heads, N = 128 dims, K = 128 keys)
 // One CTA (8 warps) owns one query row at a time: threads k and k + 128 dequantise the two
 // halves of key row k of the chunk exactly into f16 core matrices in shared memory (the
-// same bytes serve as K for S and, read MN-major, as V for O), one thread issues the MMAs,
-// the accumulators live in TMEM (key row / output dim k <-> TMEM lane k; the two threads of
-// a lane take 32 heads each), and the softmax is online across chunks with the O and l
-// accumulators rescaled in TMEM when a head's running maximum grows.
+// same bytes serve as K, K-major, for S and, read MN-major, as V for O), one thread issues
+// the MMAs, and both accumulators live in TMEM.  An M = 64 accumulator puts head h in TMEM
+// lane 32 (h / 16) + h % 16, so lanes 0-15 of each warp hold 16 heads' rows: each head's
+// softmax is thread-local, shared by two threads (warps w and w + 4), one per half of the
+// chunk's keys and one per half of the output dims.  The softmax is online across chunks:
+// a head's running maximum, its rescaling of O in TMEM and its row sum (the same
+// f16-rounded P the product uses, added in float32) all stay with the head's threads.
 //
-// Shared-memory operands use the no-swizzle core-matrix layout: 8 rows x 16 bytes per
-// 128-byte core matrix; for K-major operands the descriptor's leading offset is the stride
-// between core matrices along K and the stride offset the stride along M/N; for MN-major
-// operands the same roles hold (leading = along K, stride = along M/N).
 #include <cfloat>
 
 #include "common.cuh"
@@ -27,19 +25,18 @@
 
 namespace csa2 {
 
-constexpr int kTcThreads = 256;          // 8 warps: threads k and k + 128 <-> key row k <-> TMEM lane k
-constexpr int kTcChunk = 128;            // key rows per chunk (MMA M)
-constexpr int kTcMaxH = 64;              // heads handled per CTA (MMA N)
-constexpr int kTcCols = 256;             // TMEM columns per CTA: S | O^T | l
+constexpr int kTcThreads = 256;          // 8 warps: threads k and k + 128 dequantise key row k
+constexpr int kTcChunk = 128;            // key rows per chunk (N of S, K of P V)
+constexpr int kTcMaxH = 64;              // heads per row (M of both products)
+constexpr int kTcCols = 256;             // TMEM columns per CTA: S (128 keys) | O (128 dims)
 constexpr float kTcLog2e = 1.4426950408889634f;
 
-// dynamic shared memory layout (bytes)
-constexpr int kTcQ = 0;                                   // Q: (hg, dg) blocks, H x 128 f16   16 KB
-constexpr int kTcK = kTcQ + kTcMaxH * kD * 2;             // K chunk: (kg, dg) blocks          32 KB
-constexpr int kTcP = kTcK + kTcChunk * kD * 2;            // P^T: (kg, hg) blocks              16 KB
-constexpr int kTcP2 = kTcP + kTcChunk * kTcMaxH * 2;      // P^T without the FP8 row scale    16 KB
-constexpr int kTcOnes = kTcP2 + kTcChunk * kTcMaxH * 2;   // one core matrix of f16 ones      128 B
-constexpr int kTcSmem = kTcOnes + 128;
+// dynamic shared memory layout (bytes); every operand is K-major (V: MN-major) in 8 x 16-byte
+// core matrices, block (group of 8 rows, group of 8 K elements) at group * 2048 + kgroup * 128
+constexpr int kTcQ = 0;                                   // Q: 64 heads x 128 dims f16         16 KB
+constexpr int kTcK = kTcQ + kTcMaxH * kD * 2;             // K chunk: 128 keys x 128 dims f16   32 KB
+constexpr int kTcP = kTcK + kTcChunk * kD * 2;            // P: 64 heads x 128 keys f16         16 KB
+constexpr int kTcSmem = kTcP + kTcMaxH * kTcChunk * 2;
 // padding that keeps at most two CTAs on an SM (their TMEM columns fit: 2 x 256 = 512)
 constexpr int kTcSmemLaunch = 96 * 1024;
 static_assert(kTcSmem <= kTcSmemLaunch, "layout");
@@ -165,16 +162,18 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
   extern __shared__ __align__(1024) uint8_t s_dyn[];
   __shared__ __align__(8) uint64_t s_mbar[2];               // S done, P V done
   __shared__ uint32_t s_tmem;
-  __shared__ float s_red[4][kTcMaxH];
-  __shared__ float s_m[kTcMaxH], s_alpha[kTcMaxH];
-  __shared__ int s_rescale;
+  __shared__ __align__(16) float s_kmul[kTcChunk];          // per key of the chunk: score factor (log2 domain)
+  __shared__ __align__(16) float s_kval[kTcChunk];          //   and value factor (< 0: not a valid key)
+  __shared__ float s_cmax[2][kTcMaxH];                      // chunk maxima of the two key halves
+  __shared__ float s_lsum[2][kTcMaxH];                      // row sums of the two key halves
   pdl_enter();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int k = tid & (kTcChunk - 1), half = tid >> 7;      // key row / TMEM lane / dim, and head-dim half
+  const int k = tid & (kTcChunk - 1), half = tid >> 7;      // dequantiser role: key row k, dims half
   const int H = a.H;                                         // <= kTcMaxH, a multiple of 16
-  const int h_lo = 32 * half;                                // this thread's heads: h_lo .. h_lo + 31
-  const bool heads = h_lo < H;
-  uint8_t *qs = s_dyn + kTcQ, *ks = s_dyn + kTcK, *ps = s_dyn + kTcP, *ps2 = s_dyn + kTcP2;
+  // softmax role (lanes 0-15): head m, keys / output dims half kh
+  const int kh = warp >> 2, m = 16 * (warp & 3) + lane;
+  const bool own = lane < 16 && m < H;
+  uint8_t *qs = s_dyn + kTcQ, *ks = s_dyn + kTcK, *ps = s_dyn + kTcP;
   const uint32_t mb_s = smem_addr(&s_mbar[0]), mb_pv = smem_addr(&s_mbar[1]);
 
   if (tid == 0) {
@@ -182,20 +181,22 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
     asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(mb_pv));
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
-  if (tid < 64) reinterpret_cast<__half *>(s_dyn + kTcOnes)[tid] = __float2half(1.f);
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(smem_addr(&s_tmem)),
                  "r"(kTcCols));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
   }
+  // queries of heads >= H stay zero (their rows of S and O are never read)
+  for (int i = tid; i < kTcMaxH * kD * 2 / 16; i += kTcThreads) reinterpret_cast<uint4 *>(qs)[i] = make_uint4(0, 0, 0, 0);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  const uint32_t t_s = tmem, t_o = tmem + kTcMaxH, t_l = tmem + 2 * kTcMaxH;
-  const uint32_t lane_off = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's TMEM lanes
-  const uint32_t id_s = umma_idesc(kTcChunk, H, 0, 0);       // S^T = K Q^T
-  const uint32_t id_o = umma_idesc(kD, H, 1, 1);             // O^T += V^T P^T, l += 1 P^T
+  const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;   // this warp's TMEM lanes
+  const uint32_t t_s = tmem + lane_base + 64 * kh;                // this thread's 64 keys of S
+  const uint32_t t_o = tmem + lane_base + kTcChunk + 64 * kh;     // this thread's 64 dims of O
+  const uint32_t id_s = umma_idesc(kTcMaxH, kTcChunk, 0, 0);      // S = Q K^T: A, B K-major
+  const uint32_t id_o = umma_idesc(kTcMaxH, kD, 0, 1);            // O += P V: A K-major, B MN-major
   uint32_t ph_s = 0, ph_pv = 0;
   bool pv_pending = false, dead = false;   // dead: a wait ran out (uniform across the CTA)
   const float ltau = a.tau * kTcLog2e;
@@ -242,7 +243,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
             make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
     }
-    if (tid < kTcMaxH) s_m[tid] = -INFINITY;
+    float run_m = -INFINITY, lsum = 0.f;                     // this head's running maximum and row sum
 
     for (int c = 0; c < a.n_chunks; ++c) {
       // ---- K and P are free once the previous P V product has completed
@@ -254,8 +255,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
         tc_fence_after();
       }
       store_key(ks, k, half, kr);
-      const bool fp8 = kr.fp8, valid = kr.valid;
-      const float wsc = kr.wsc;
+      if (half == 0) {
+        s_kmul[k] = kr.valid ? (kr.fp8 ? ltau * kr.wsc : ltau) : 0.f;
+        s_kval[k] = kr.valid ? (kr.fp8 ? kr.wsc : 1.f) : -1.f;
+      }
       if (c + 1 < a.n_chunks) {                              // the next chunk's rows
         int64_t rp;
         key_slot(a, c + 1, k, t, 0, false, p, kr, rp);
@@ -269,7 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
       if (tid == 0) {
 #pragma unroll
         for (int s = 0; s < kD / 16; ++s)
-          umma_f16(t_s, umma_desc(smem_addr(ks) + 256 * s, 128, 2048), umma_desc(smem_addr(qs) + 256 * s, 128, 2048),
+          umma_f16(tmem, umma_desc(smem_addr(qs) + 256 * s, 128, 2048), umma_desc(smem_addr(ks) + 256 * s, 128, 2048),
                    id_s, s > 0);
         umma_commit(mb_s);
       }
@@ -278,69 +281,70 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
       ph_s ^= 1u;
       tc_fence_after();
 
-      // ---- scores of this key row for this thread's heads; chunk maxima per head
-      const float rs = fp8 ? ltau * wsc : ltau;                // log2-domain scale of this row's scores
-      float sv[32];
+      // ---- this head's scores of its 64 keys (log2 domain); the chunk maximum
+      float sv[64];
       {
         float v[32];
-        if (heads) tmem_ld32(t_s + lane_off + h_lo, v);
+        tmem_ld32(t_s, v);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) sv[j] = (heads && h_lo + j < H && valid) ? v[j] * rs : -INFINITY;
-      }
+        for (int j = 0; j < 32; ++j) sv[j] = v[j];
+        tmem_ld32(t_s + 32, v);
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float m = warp_max_f32(sv[j]);
-        if (lane == j) s_red[warp & 3][h_lo + j] = m;
+        for (int j = 0; j < 32; ++j) sv[32 + j] = v[j];
       }
+      float cm = -INFINITY;
+#pragma unroll
+      for (int j4 = 0; j4 < 16; ++j4) {
+        const float4 km = *reinterpret_cast<const float4 *>(&s_kmul[64 * kh + 4 * j4]);
+        const float4 kv = *reinterpret_cast<const float4 *>(&s_kval[64 * kh + 4 * j4]);
+        sv[4 * j4 + 0] = kv.x >= 0.f ? sv[4 * j4 + 0] * km.x : -INFINITY;
+        sv[4 * j4 + 1] = kv.y >= 0.f ? sv[4 * j4 + 1] * km.y : -INFINITY;
+        sv[4 * j4 + 2] = kv.z >= 0.f ? sv[4 * j4 + 2] * km.z : -INFINITY;
+        sv[4 * j4 + 3] = kv.w >= 0.f ? sv[4 * j4 + 3] * km.w : -INFINITY;
+        cm = fmaxf(cm, fmaxf(fmaxf(sv[4 * j4], sv[4 * j4 + 1]), fmaxf(sv[4 * j4 + 2], sv[4 * j4 + 3])));
+      }
+      if (lane < 16) s_cmax[kh][m] = cm;
       if (__syncthreads_or(!s_done)) { dead = true; break; }
-      if (tid < H) {
-        const float m_old = s_m[tid];
-        const float m_new = fmaxf(m_old, fmaxf(fmaxf(s_red[0][tid], s_red[1][tid]), fmaxf(s_red[2][tid], s_red[3][tid])));
-        s_alpha[tid] = (m_old == -INFINITY || m_old == m_new) ? 1.f : exp2f(m_old - m_new);
-        s_m[tid] = m_new;
-      }
-      if (tid == 0) s_rescale = 0;
-      __syncthreads();
-      if (tid < H && s_alpha[tid] != 1.f) s_rescale = 1;
+      const float m_new = fmaxf(run_m, fmaxf(s_cmax[0][m & (kTcMaxH - 1)], s_cmax[1][m & (kTcMaxH - 1)]));
+      const float alpha = (run_m == -INFINITY || run_m == m_new) ? 1.f : exp2f(run_m - m_new);
+      run_m = m_new;
 
-      // ---- P^T row of this key (f16).  A window row's values are its E4M3 codes, so its
-      // float32 scale multiplies P for O; the row sums take P without it (second copy).
-      if (heads) {
+      // ---- P (f16) of this head's keys into the A operand; the row sum adds the same f16 P
+      // (a window row's float32 scale multiplies P for O only)
+      if (own) {
+        float ls = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (h_lo + 8 * q < H) {
-            float pr[8];
+        for (int g = 0; g < 8; ++g) {                          // keys 64 kh + 8 g .. + 7
+          uint32_t w4[4];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float x = sv[8 * q + j];
-              pr[j] = x == -INFINITY ? 0.f : exp2f(x - s_m[h_lo + 8 * q + j]);
-            }
-            const int off = ((k >> 3) * (kTcMaxH / 8) + (h_lo >> 3) + q) * 128 + (k & 7) * 16;
-            if (fp8) {
-              *reinterpret_cast<uint4 *>(ps2 + off) = make_uint4(pack_f16x2(pr[0], pr[1]), pack_f16x2(pr[2], pr[3]),
-                                                                 pack_f16x2(pr[4], pr[5]), pack_f16x2(pr[6], pr[7]));
-#pragma unroll
-              for (int j = 0; j < 8; ++j) pr[j] *= wsc;
-            }
-            *reinterpret_cast<uint4 *>(ps + off) = make_uint4(pack_f16x2(pr[0], pr[1]), pack_f16x2(pr[2], pr[3]),
-                                                              pack_f16x2(pr[4], pr[5]), pack_f16x2(pr[6], pr[7]));
+          for (int j = 0; j < 4; ++j) {
+            const int i0 = 8 * g + 2 * j;
+            const float p0 = sv[i0] == -INFINITY ? 0.f : exp2f(sv[i0] - m_new);
+            const float p1 = sv[i0 + 1] == -INFINITY ? 0.f : exp2f(sv[i0 + 1] - m_new);
+            const __half2 h2 = __floats2half2_rn(p0, p1);
+            const float2 f2 = __half22float2(h2);
+            ls += f2.x + f2.y;
+            const float v0 = s_kval[64 * kh + i0], v1 = s_kval[64 * kh + i0 + 1];
+            w4[j] = (v0 == 1.f && v1 == 1.f) ? *reinterpret_cast<const uint32_t *>(&h2)
+                                             : pack_f16x2(p0 * fmaxf(v0, 0.f), p1 * fmaxf(v1, 0.f));
           }
+          const int kg = 8 * kh + g;                           // key group of the chunk
+          *reinterpret_cast<uint4 *>(ps + ((m >> 3) * 16 + kg) * 128 + (m & 7) * 16) =
+              make_uint4(w4[0], w4[1], w4[2], w4[3]);
         }
+        lsum = lsum * alpha + ls;
       }
-      __syncthreads();
-      // ---- a head's maximum grew: rescale its O^T column and its row sum
-      if (c > 0 && s_rescale && heads) {
-        float v[32], u[32];
-        tmem_ld32(t_o + lane_off + h_lo, v);
-        tmem_ld32(t_l + lane_off + h_lo, u);
+      // ---- a head's maximum grew: rescale its O row (this thread's 64 dims); the TMEM
+      // access is warp-wide, so the warp rescales when any of its heads needs it
+      if (c > 0 && __any_sync(0xffffffffu, own && alpha != 1.f)) {
+        float v[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float al = s_alpha[h_lo + j];
-          v[j] *= al;
-          u[j] *= al;
+        for (int hh = 0; hh < 2; ++hh) {
+          tmem_ld32(t_o + 32 * hh, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] *= alpha;
+          tmem_st32(t_o + 32 * hh, v);
         }
-        tmem_st32(t_o + lane_off + h_lo, v);
-        tmem_st32(t_l + lane_off + h_lo, u);
         tmem_st_wait();
       }
       fence_async_smem();
@@ -348,16 +352,10 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
       __syncthreads();
       tc_fence_after();
       if (tid == 0) {
-        const uint32_t pl = smem_addr(c >= a.n_sel_chunks ? ps2 : ps);   // P for the row sums
 #pragma unroll
-        for (int s = 0; s < kTcChunk / 16; ++s) {
-          const uint32_t koff = 2 * (kTcMaxH / 8) * 128 * s;
-          const uint64_t bd = umma_desc(smem_addr(ps) + koff, (kTcMaxH / 8) * 128, 128);
-          const uint64_t bl = umma_desc(pl + koff, (kTcMaxH / 8) * 128, 128);
-          const uint32_t acc = (c > 0 || s > 0) ? 1u : 0u;
-          umma_f16(t_o, umma_desc(smem_addr(ks) + 2 * 2048 * s, 2048, 128), bd, id_o, acc);
-          umma_f16(t_l, umma_desc(smem_addr(s_dyn + kTcOnes), 0, 0), bl, id_o, acc);
-        }
+        for (int s = 0; s < kTcChunk / 16; ++s)
+          umma_f16(tmem + kTcChunk, umma_desc(smem_addr(ps) + 256 * s, 128, 2048),
+                   umma_desc(smem_addr(ks) + 2 * 2048 * s, 2048, 128), id_o, (c > 0 || s > 0) ? 1u : 0u);
         umma_commit(mb_pv);
       }
       __syncwarp();
@@ -365,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
     }
 
     if (dead) break;
-    // ---- O = O^T / l: thread (d, half) holds dim d of heads h_lo .. h_lo + 31
+    // ---- O / l: thread (m, kh) writes dims 64 kh .. 64 kh + 63 of head m
     bool waited = true;
     if (pv_pending) {
       waited = mbar_wait(mb_pv, ph_pv);
@@ -373,24 +371,25 @@ __global__ void __launch_bounds__(kTcThreads, 2) attn_chunked_tc_kernel(const __
       pv_pending = false;
       tc_fence_after();
     }
+    if (lane < 16) s_lsum[kh][m] = lsum;
     if (__syncthreads_or(!waited)) { dead = true; break; }
-    const int64_t head0 = (int64_t)t * H;
-    if (heads) {
-      float v[32], u[32];
-      tmem_ld32(t_o + lane_off + h_lo, v);
-      tmem_ld32(t_l + lane_off + h_lo, u);
+    const float l = s_lsum[0][m & (kTcMaxH - 1)] + s_lsum[1][m & (kTcMaxH - 1)];
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+    float *orow = a.out + ((int64_t)t * H + m) * kD + 64 * kh;
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        if (h_lo + j < H) {
-          const float l = u[j];                               // every lane holds every head's sum
-          a.out[(head0 + h_lo + j) * kD + k] = l > 0.f ? v[j] / l : 0.f;
-          if (a.lse && k == j)
-            a.lse[head0 + h_lo + j] = l > 0.f ? s_m[h_lo + j] / kTcLog2e + logf(l) : -INFINITY;
-        }
+    for (int hh = 0; hh < 2; ++hh) {
+      float v[32];
+      tmem_ld32(t_o + 32 * hh, v);
+      if (own) {
+#pragma unroll
+        for (int j = 0; j < 32; j += 4)
+          *reinterpret_cast<float4 *>(orow + 32 * hh + j) =
+              make_float4(v[j] * inv, v[j + 1] * inv, v[j + 2] * inv, v[j + 3] * inv);
       }
     }
+    if (own && kh == 0 && a.lse) a.lse[(int64_t)t * H + m] = l > 0.f ? run_m / kTcLog2e + logf(l) : -INFINITY;
     tc_fence_before();
-    __syncthreads();                                          // s_m and TMEM reads done before the next row
+    __syncthreads();                                          // TMEM reads and s_lsum done before the next row
     tc_fence_after();
   }
   if (dead && tid == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT);
