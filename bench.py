@@ -45,9 +45,9 @@ SCAN_SCORE_STORE = 4             # the scan's own per-position score store (scra
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one scan launch, from one ncu
 # capture of the decode batch, valid only while the scan's sources are the ones captured: the
 # digest covers them, and any change reports the traffic as null.
-SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142720256 + 5331968}
+SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142737664 + 6975232}
 SCAN_NCU_SOURCES = ("sparse_attention_fp4_02_b300/csrc/indexer.cu", "sparse_attention_fp4_02_b300/csrc/common.cuh")
-SCAN_NCU_DIGEST = "6e1fe76be3c29af4dba078e43ca6062e7a29f4518edbbfd33b946172f3e62a99"
+SCAN_NCU_DIGEST = "71625017a6a42ccef782e57ab8ec037074724d701efc9c9ef7d9f800c5fb17bb"
 
 
 def scan_traffic(workload: str):
