@@ -499,7 +499,7 @@ cudaError_t launch_attn_decode(const csa2_cache &c, const csa2_swa &swa, const u
                                int window, float tau, float *out, float *lse, void *, int32_t *d_err,
                                cudaStream_t st) {
   if (T == 0) return cudaSuccess;
-  if (attn_tc_eligible(T, H))
+  if (attn_tc_eligible(T, H) && topk + window > 0)
     return launch_attn_chunked_tc(c, swa, q, H, T, q_seq, q_pos, topk_idx, topk, window, tau, out, lse, d_err, st);
   opt_in_smem((const void *)attn_decode_kernel, attn_smem(kMaxSplit), kSiteAttnOptin, 0);
   AttnArgs a;
