@@ -37,14 +37,16 @@ __device__ __forceinline__ void umma_commit(uint32_t mbar) {
                : "memory");
 }
 
-// Bounded wait on an mbarrier phase; false if it did not complete in time.
+// Bounded wait on an mbarrier phase; false if it did not complete in time.  Each try
+// suspends the thread for up to 1 us (the suspend-time hint) instead of returning at once,
+// so that waiting warps do not take issue slots from the working warps of their scheduler.
 __device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
   for (int it = 0; it < (1 << 20); ++it) {
     uint32_t done;
     asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(done)
-        : "r"(mbar), "r"(parity)
+        : "r"(mbar), "r"(parity), "r"(1000u)
         : "memory");
     if (done) return true;
   }
