@@ -47,7 +47,7 @@ SCAN_SCORE_STORE = 4             # the scan's own per-position score store (scra
 # digest covers them, and any change reports the traffic as null.
 SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142737664 + 6975232}
 SCAN_NCU_SOURCES = ("sparse_attention_fp4_02_b300/csrc/indexer.cu", "sparse_attention_fp4_02_b300/csrc/common.cuh")
-SCAN_NCU_DIGEST = "71625017a6a42ccef782e57ab8ec037074724d701efc9c9ef7d9f800c5fb17bb"
+SCAN_NCU_DIGEST = "a50fb76dda3dc0b46311a0e21954d99404226223c9558bec7bdd17ba9f524e1a"
 
 
 def scan_traffic(workload: str):

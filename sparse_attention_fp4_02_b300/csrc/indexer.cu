@@ -644,7 +644,7 @@ __global__ void __launch_bounds__(kScanWarps * 32, CSA2_SCAN_CTAS)
   uint32_t *hist = a.ws.hist + (int64_t)cb * kHistBins;
   bool home = cb == home_b;
   auto consume = [&](int k) {
-    const bool landed = mbar_wait(smem_addr(&s_full[warp][k & (kScanStages - 1)]), (k / kScanStages) & 1);
+    const bool landed = mbar_wait_spin(smem_addr(&s_full[warp][k & (kScanStages - 1)]), (k / kScanStages) & 1);
     if (!landed && lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT);
     cp_async_wait<kScanStages - 1>();
     __syncwarp();
