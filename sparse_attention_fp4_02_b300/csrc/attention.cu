@@ -171,12 +171,14 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     set_err(a.d_err, (b < 0 || b >= a.c.B) ? CSA2_DEVERR_SEQ : CSA2_DEVERR_POS);
 
   // ---- queries (bf16 -> f16 into shared memory); their loads overlap the first gathers
-  constexpr int kQPer = 256 / (kAttnWarps * 32);                    // 16 heads x 16 chunks of 8 values
+  // 16 heads x 16 chunks of 8 values: kQPer per thread (threads beyond 256 load none)
+  constexpr int kQPer = (256 + kAttnWarps * 32 - 1) / (kAttnWarps * 32);
   uint4 qv[kQPer];
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
     const int i = tid + j * kAttnWarps * 32, h = i >> 4, c8 = i & 15;
-    qv[j] = __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8));
+    qv[j] = i < 256 ? __ldg(reinterpret_cast<const uint4 *>(a.q + ((int64_t)t * a.H + 16 * hg + h) * kD + 8 * c8))
+                    : make_uint4(0, 0, 0, 0);
   }
 
   // ---- this warp's tiles: the row's tiles are split evenly over every warp of the cluster
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
 #pragma unroll
   for (int j = 0; j < kQPer; ++j) {
     const int i = tid + j * kAttnWarps * 32, h = i >> 4, c8 = i & 15;
+    if (i >= 256) break;
     const uint32_t w[4] = {qv[j].x, qv[j].y, qv[j].z, qv[j].w};
     uint32_t o4[4];
 #pragma unroll

@@ -2,13 +2,13 @@
 //
 // Method: the Full layer's indexer score (origotech.dev deep dive, subsection "Compressed
 // Sparse Attention 2(CSA2)"), sigma_t = s_t * sum_h w_h * max(q_h . k_t, 0), for many query
-// rows of one session at once.  Sixteen rows share every key, so their 16 x 8 head queries
-// form the N = 128 side of one dense contraction per tile of 128 keys:
-//   D = K Q^T      (M = 128 keys, N = 16 rows x 8 heads, K = 64 dims)
+// rows of one session at once.  Thirty-two rows share every key, so their 32 x 8 head
+// queries form the N = 256 side of one dense contraction per tile of 128 keys:
+//   D = K Q^T      (M = 128 keys, N = 32 rows x 8 heads, K = 64 dims)
 // The E4M3 keys are converted exactly to f16 into shared-memory core matrices, the queries
 // are scaled per (row, head) by the same power of two as in the one-query scan (so the same
 // certified error bound holds), D accumulates in TMEM, and the epilogue (thread <-> key,
-// four rows per thread) forms ReLU * w, the key scale, the block maxima and their
+// eight rows per thread in two passes of four) forms ReLU * w, the key scale, the block maxima and their
 // histogram, and stores every position's score for the exact selection that follows.
 // A row only counts the positions up to its own (its length in the row view).
 //
@@ -24,20 +24,20 @@
 
 namespace csa2 {
 
-constexpr int kCqRows = 16;                                // query rows per group
+constexpr int kCqRows = 32;                                // query rows per group
 constexpr int kCqKeys = 128;                               // keys per tile (MMA M)
-constexpr int kCqN = kCqRows * kHIdx;                      // MMA N = 128
+constexpr int kCqN = kCqRows * kHIdx;                      // MMA N = 256
 constexpr int kCqThreads = 512;                            // 16 warps: 4 per TMEM lane quarter
 constexpr int kCqCols = 2 * kCqN;                          // TMEM: two accumulators
 constexpr int kCqTileBytes = kCqKeys * kDIdx * 2;          // 16 KB of f16 keys
-constexpr int kCqQ = 0;                                    // Q: 128 x 64 f16, 16 KB
+constexpr int kCqQ = 0;                                    // Q: 256 x 64 f16, 32 KB
 constexpr int kCqK = kCqQ + kCqN * kDIdx * 2;              // two key tiles
-constexpr int kCqSmem = kCqK + 2 * kCqTileBytes;           // 48 KB
-constexpr int kCqSmemLaunch = 80 * 1024;                   // one CTA per SM (also set by its registers)
+constexpr int kCqSmem = kCqK + 2 * kCqTileBytes;           // 64 KB
+constexpr int kCqSmemLaunch = 96 * 1024;                   // one CTA per SM (also set by its registers and TMEM)
 constexpr int kCqMaxGroups = CSA2_MAX_B / kCqRows;
 constexpr int kCqRowGroupBytes = (kDIdx / 8) * 128;        // 8 rows x 64 dims: 8 core matrices
 static_assert(kCqSmem <= kCqSmemLaunch, "layout");
-static_assert(kCqN == 128, "one accumulator is 128 columns");
+static_assert(kCqN == 256, "one accumulator is 256 columns");
 
 // Byte offset of (row n, dims 8kg..8kg+7) in a K-major no-swizzle operand of 64 dims.
 __device__ __forceinline__ int cq_off(int n, int kg) { return (n >> 3) * kCqRowGroupBytes + kg * 128 + (n & 7) * 16; }
@@ -63,7 +63,7 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
   __shared__ int64_t s_first[kCqMaxGroups + 1];              // first item of each group
   __shared__ int64_t s_base[kCqMaxGroups];
   __shared__ int32_t s_maxlen[kCqMaxGroups];
-  __shared__ float s_wi[kCqRows][kHIdx];                      // w * 2^-c of the current group
+  __shared__ __align__(16) float s_wi[kCqRows][kHIdx];       // w * 2^-c of the current group
   __shared__ int32_t s_len[kCqRows];                          // lengths of the current group's rows
   pdl_enter();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -138,21 +138,16 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
     xs = v ? __ldg(a.ik_scale + row) : 0.f;
   };
 
-  // the current group's rows of this thread: weights, lengths, score rows
-  float wr[4][kHIdx] = {};
-  int32_t lenr[4];
-  float *rowp[4];
-  float *bmaxp[4];
-  uint32_t *histp[4];
-  float smx[4];                                               // per row: largest valid key scale seen
+  // the current group's rows of this thread (8 eq .. 8 eq + 7): largest valid key scale seen
+  float smx[8];
 #pragma unroll
-  for (int j = 0; j < 4; ++j) { smx[j] = 0.f; lenr[j] = 0; rowp[j] = a.ws.sigma; bmaxp[j] = a.ws.bmax; histp[j] = a.ws.hist; }
+  for (int j = 0; j < 8; ++j) smx[j] = 0.f;
   int cur_g = -1;
   auto flush_smax = [&]() {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < 8; ++j) {
       const float m = warp_max(smx[j]);
-      const int r = cur_g * kCqRows + 4 * eq + j;
+      const int r = cur_g * kCqRows + 8 * eq + j;
       if (lane == 0 && r < a.n && m > 0.f) atomicMax(&a.ws.smax[r], __float_as_uint(m));
       smx[j] = 0.f;
     }
@@ -172,48 +167,55 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
     if (pend_buf) ph1 ^= 1u; else ph0 ^= 1u;
     tc_fence_after();
     if (!ok) { dead = true; if (lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT); return; }
-    float v[32];
-    tmem_ld32(tmem + lane_off + pend_buf * kCqN + 32 * eq, v);
     const int em = 32 * (warp & 3) + lane;                    // == km
     const int kk = (int)pend_tile * kCqKeys + em;             // < 2^31: positions of one row
-    float bm[4];
-    bool bv[4];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      float acc = 0.f;
+    for (int pass = 0; pass < 2; ++pass) {                    // rows 8 eq + 4 pass + j
+      float v[32];
+      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eq + 32 * pass, v);
+      float bm[4];
+      bool bv[4];
 #pragma unroll
-      for (int h = 0; h < kHIdx; ++h) acc = fmaf(fmaxf(v[8 * j + h], 0.f), wr[j][h], acc);
-      float o = acc * pend_ks;
-      o = o > 0.f ? o : 0.f;                                  // also maps NaN and -0 to +0
-      const bool valid = kk < lenr[j];
-      if (valid) rowp[j][kk] = o;
-      smx[j] = fmaxf(smx[j], valid ? pend_ks : 0.f);
-      float m = valid ? o : 0.f;
+      for (int j = 0; j < 4; ++j) {
+        const int jr = 8 * eq + 4 * pass + j;
+        const float4 w0 = *reinterpret_cast<const float4 *>(&s_wi[jr][0]);
+        const float4 w1 = *reinterpret_cast<const float4 *>(&s_wi[jr][4]);
+        const float wv[kHIdx] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+        float acc = 0.f;
 #pragma unroll
-      for (int s = 1; s < BLOCK; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-      bm[j] = m;                                              // the block's maximum, in every lane of it
-      bv[j] = __shfl_sync(0xffffffffu, valid, lane & ~(BLOCK - 1));   // its first position is valid
-    }
-    // lane i of a block writes row i's maximum (BLOCK >= 4), or the block's first lane all four
-    if (BLOCK >= 4) {
-      const int jj = em & (BLOCK - 1);
-      if (jj < 4) {
-        const float m = jj == 0 ? bm[0] : jj == 1 ? bm[1] : jj == 2 ? bm[2] : bm[3];
-        const bool ok = jj == 0 ? bv[0] : jj == 1 ? bv[1] : jj == 2 ? bv[2] : bv[3];
-        if (ok) {
-          float *bp = jj == 0 ? bmaxp[0] : jj == 1 ? bmaxp[1] : jj == 2 ? bmaxp[2] : bmaxp[3];
-          uint32_t *hp = jj == 0 ? histp[0] : jj == 1 ? histp[1] : jj == 2 ? histp[2] : histp[3];
-          bp[(kk - jj) / BLOCK] = m;
-          atomicAdd(&hp[min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
-        }
+        for (int h = 0; h < kHIdx; ++h) acc = fmaf(fmaxf(v[8 * j + h], 0.f), wv[h], acc);
+        float o = acc * pend_ks;
+        o = o > 0.f ? o : 0.f;                                // also maps NaN and -0 to +0
+        const bool valid = kk < s_len[jr];
+        if (valid) a.ws.sigma[((int64_t)cur_g * kCqRows + jr) * a.ws.sigma_stride + kk] = o;
+        smx[4 * pass + j] = fmaxf(smx[4 * pass + j], valid ? pend_ks : 0.f);
+        float m = valid ? o : 0.f;
+#pragma unroll
+        for (int s = 1; s < BLOCK; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
+        bm[j] = m;                                            // the block's maximum, in every lane of it
+        bv[j] = __shfl_sync(0xffffffffu, valid, lane & ~(BLOCK - 1));   // its first position is valid
       }
-    } else {
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        if ((em % BLOCK) == 0 && bv[j]) {
-          bmaxp[j][kk / BLOCK] = bm[j];
-          atomicAdd(&histp[j][min(__float_as_uint(bm[j]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+      // lane i of a block writes row i's maximum (BLOCK >= 4), or the block's first lane all four
+      if (BLOCK >= 4) {
+        const int jj = em & (BLOCK - 1);
+        if (jj < 4) {
+          const float m = jj == 0 ? bm[0] : jj == 1 ? bm[1] : jj == 2 ? bm[2] : bm[3];
+          const bool ok = jj == 0 ? bv[0] : jj == 1 ? bv[1] : jj == 2 ? bv[2] : bv[3];
+          if (ok) {
+            const int64_t r = (int64_t)cur_g * kCqRows + 8 * eq + 4 * pass + jj;
+            a.ws.bmax[r * a.ws.nbm + (kk - jj) / BLOCK] = m;
+            atomicAdd(&a.ws.hist[r * kHistBins + min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+          }
         }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if ((em % BLOCK) == 0 && bv[j]) {
+            const int64_t r = (int64_t)cur_g * kCqRows + 8 * eq + 4 * pass + j;
+            a.ws.bmax[r * a.ws.nbm + kk / BLOCK] = bm[j];
+            atomicAdd(&a.ws.hist[r * kHistBins + min(__float_as_uint(bm[j]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
+          }
+      }
     }
   };
 
@@ -229,20 +231,23 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
       if (pend) { epilogue(); pend = false; }
       if (cur_g >= 0) flush_smax();
       if (__syncthreads_or(dead)) break;
-      // queries of group g: (row jr, head h) = MMA column n = 8 jr + h; four threads per pair
-      const int pair = tid >> 2, part = tid & 3;
-      const int jr = pair >> 3, h = pair & 7;
-      const int r = g * kCqRows + jr;
-      const bool rv = r < a.n;
-      uint32_t wq[8];
-      if (rv) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * kHIdx + h) * kDIdx + 16 * part);
-        const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
-        wq[0] = u0.x; wq[1] = u0.y; wq[2] = u0.z; wq[3] = u0.w;
-        wq[4] = u1.x; wq[5] = u1.y; wq[6] = u1.z; wq[7] = u1.w;
-      } else {
+      // queries of group g: (row jr, head h) = MMA column n = 8 jr + h; four threads per pair,
+      // two pairs per thread
 #pragma unroll
-        for (int i = 0; i < 8; ++i) wq[i] = 0u;
+      for (int pit = 0; pit < kCqN / (kCqThreads / 4); ++pit) {
+        const int pair = (tid >> 2) + (kCqThreads / 4) * pit, part = tid & 3;
+        const int jr = pair >> 3, h = pair & 7;
+        const int r = g * kCqRows + jr;
+        const bool rv = r < a.n;
+        uint32_t wq[8];
+        if (rv) {
+          const uint4 *src = reinterpret_cast<const uint4 *>(a.q + ((int64_t)r * kHIdx + h) * kDIdx + 16 * part);
+          const uint4 u0 = __ldg(src), u1 = __ldg(src + 1);
+          wq[0] = u0.x; wq[1] = u0.y; wq[2] = u0.z; wq[3] = u0.w;
+          wq[4] = u1.x; wq[5] = u1.y; wq[6] = u1.z; wq[7] = u1.w;
+        } else {
+  #pragma unroll
+          for (int i = 0; i < 8; ++i) wq[i] = 0u;
       }
       float mx = 0.f;
 #pragma unroll
@@ -263,6 +268,7 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
         *reinterpret_cast<uint4 *>(qs + cq_off(pair, 2 * part + i)) = make_uint4(o4[0], o4[1], o4[2], o4[3]);
       }
       if (part == 0) s_wi[jr][h] = rv ? __ldg(a.w + (int64_t)r * kHIdx + h) * pow2f(-c) : 0.f;
+      }
       if (tid < kCqRows) s_len[tid] = (g * kCqRows + tid < a.n) ? a.len_v[g * kCqRows + tid] : 0;
       cur_g = g;
     }
@@ -282,19 +288,6 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
     tc_fence_before();
     if (__syncthreads_or(dead)) break;
     tc_fence_after();
-    if (newg) {                                               // this thread's rows of the new group
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int jr = 4 * eq + j;
-        lenr[j] = s_len[jr];
-        const int64_t r = (int64_t)g * kCqRows + jr;
-        rowp[j] = a.ws.sigma + r * a.ws.sigma_stride;
-        bmaxp[j] = a.ws.bmax + r * a.ws.nbm;
-        histp[j] = a.ws.hist + r * kHistBins;
-#pragma unroll
-        for (int h = 0; h < kHIdx; ++h) wr[j][h] = s_wi[jr][h];
-      }
-    }
     if (tid == 0) {
       const uint32_t kb_a = ks_a + buf * kCqTileBytes;
 #pragma unroll
