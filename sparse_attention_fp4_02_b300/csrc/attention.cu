@@ -61,11 +61,6 @@ struct AttnArgs {
   int32_t *d_err;
 };
 
-__device__ __forceinline__ uint32_t fp4x2_to_f16x2(uint32_t byte) {
-  __half2_raw h = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)(byte & 0xFFu), __NV_E2M1);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-
 __device__ __forceinline__ uint32_t hmul2_u32(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);
@@ -253,15 +248,20 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
       const uint4 c1 = *reinterpret_cast<const uint4 *>(raw + r * 64 + 32 * hf + 16);
       const uint32_t sw = *reinterpret_cast<const uint32_t *>(raw + 1024 + r * 8 + 4 * hf);
       const uint32_t cw[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      uint32_t sp[2];                                          // the four group scales as f16 pairs
+      e4m3x4_to_f16(sw, sp[0], sp[1]);
 #pragma unroll
       for (int gi = 0; gi < 4; ++gi) {
-        const uint32_t sh = e4m3x2_to_f16x2((sw >> (8 * gi)) & 0xFFu) & 0xFFFFu;
+        const uint32_t sh = (gi & 1) ? (sp[gi >> 1] >> 16) : (sp[gi >> 1] & 0xFFFFu);
         const uint32_t s2 = sh | (sh << 16);
-        uint32_t v[8];
+        uint32_t lo[4], hi[4], v[8];
+        e2m1x8_to_f16(cw[2 * gi], lo);
+        e2m1x8_to_f16(cw[2 * gi + 1], hi);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) v[k] = hmul2_u32(fp4x2_to_f16x2(cw[2 * gi] >> (8 * k)), s2);
-#pragma unroll
-        for (int k = 0; k < 4; ++k) v[4 + k] = hmul2_u32(fp4x2_to_f16x2(cw[2 * gi + 1] >> (8 * k)), s2);
+        for (int k = 0; k < 4; ++k) {
+          v[k] = hmul2_u32(lo[k], s2);
+          v[4 + k] = hmul2_u32(hi[k], s2);
+        }
         sts128(dst + 16 * gi, v[0], v[1], v[2], v[3]);
         sts128(dst + 16 * gi + 8, v[4], v[5], v[6], v[7]);
       }
@@ -272,10 +272,13 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         const uint4 w = *reinterpret_cast<const uint4 *>(raw + r * 128 + 64 * hf + 16 * c);
-        sts128(dst + 16 * c, e4m3x2_to_f16x2(w.x), e4m3x2_to_f16x2(w.x >> 16), e4m3x2_to_f16x2(w.y),
-               e4m3x2_to_f16x2(w.y >> 16));
-        sts128(dst + 16 * c + 8, e4m3x2_to_f16x2(w.z), e4m3x2_to_f16x2(w.z >> 16), e4m3x2_to_f16x2(w.w),
-               e4m3x2_to_f16x2(w.w >> 16));
+        uint32_t v[8];
+        e4m3x4_to_f16(w.x, v[0], v[1]);
+        e4m3x4_to_f16(w.y, v[2], v[3]);
+        e4m3x4_to_f16(w.z, v[4], v[5]);
+        e4m3x4_to_f16(w.w, v[6], v[7]);
+        sts128(dst + 16 * c, v[0], v[1], v[2], v[3]);
+        sts128(dst + 16 * c + 8, v[4], v[5], v[6], v[7]);
       }
       rs = a.tau * sc;
       vs = sc;
@@ -323,8 +326,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = (mn0 == -INFINITY) ? 1.f : exp2f((m0 - mn0) * kLog2e);
-    const float al1 = (mn1 == -INFINITY) ? 1.f : exp2f((m1 - mn1) * kLog2e);
+    const float al0 = (mn0 == -INFINITY) ? 1.f : ex2_approx((m0 - mn0) * kLog2e);
+    const float al1 = (mn1 == -INFINITY) ? 1.f : ex2_approx((m1 - mn1) * kLog2e);
     m0 = mn0;
     m1 = mn1;
     float pr[2][4];
@@ -332,8 +335,8 @@ __global__ void __launch_bounds__(kAttnWarps * 32) attn_decode_kernel(const __gr
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        pr[nt][k] = z[nt][k] == -INFINITY ? 0.f : exp2f((z[nt][k] - mn0) * kLog2e);
-        pr[nt][2 + k] = z[nt][2 + k] == -INFINITY ? 0.f : exp2f((z[nt][2 + k] - mn1) * kLog2e);
+        pr[nt][k] = z[nt][k] == -INFINITY ? 0.f : ex2_approx((z[nt][k] - mn0) * kLog2e);
+        pr[nt][2 + k] = z[nt][2 + k] == -INFINITY ? 0.f : ex2_approx((z[nt][2 + k] - mn1) * kLog2e);
       }
     }
     l0 = l0 * al0 + (pr[0][0] + pr[0][1] + pr[1][0] + pr[1][1]);

@@ -38,6 +38,30 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t two_codes) {
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// eight E2M1 codes (a 32-bit word, low nibble first) to four packed f16 pairs; exact
+__device__ __forceinline__ void e2m1x8_to_f16(uint32_t w, uint32_t (&o)[4]) {
+  asm("{\n .reg .b8 c0, c1, c2, c3;\n mov.b32 {c0, c1, c2, c3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, c0;\n cvt.rn.f16x2.e2m1x2 %1, c1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, c2;\n cvt.rn.f16x2.e2m1x2 %3, c3;\n}\n"
+      : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+      : "r"(w));
+}
+
+// four E4M3 codes (low byte first) to two packed f16 pairs; exact
+__device__ __forceinline__ void e4m3x4_to_f16(uint32_t w, uint32_t &o0, uint32_t &o1) {
+  asm("{\n .reg .b16 h0, h1;\n mov.b32 {h0, h1}, %2;\n cvt.rn.f16x2.e4m3x2 %0, h0;\n cvt.rn.f16x2.e4m3x2 %1, h1;\n}\n"
+      : "=r"(o0), "=r"(o1)
+      : "r"(w));
+}
+
+// 2^x from the special-function unit (ex2.approx, relative error near 2^-22); flushes
+// subnormal results to zero
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // non-negative float -> E2M1 magnitude code 0..7, nearest even, saturating at 6
 __device__ __forceinline__ uint32_t f32_to_e2m1_mag(float x) {
   return (uint32_t)__nv_cvt_float_to_fp4(x, __NV_E2M1, cudaRoundNearest) & 7u;
