@@ -105,6 +105,27 @@ __device__ __forceinline__ uint32_t hmul2_bits(uint32_t a, uint32_t b) {
   __half2 r = __hmul2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
   return *reinterpret_cast<uint32_t *>(&r);
 }
+// packed two-wide float32 arithmetic (one instruction for a key pair; each half rounds as
+// the scalar operation would)
+__device__ __forceinline__ uint64_t f2_bits(float2 a) { return ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x); }
+__device__ __forceinline__ float2 bits_f2(uint64_t r) {
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;\n" : "=l"(r) : "l"(f2_bits(a)), "l"(f2_bits(b)));
+  return bits_f2(r);
+}
 __device__ __forceinline__ void cp_async8(uint32_t dst, const void *src) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src));
 }
@@ -479,10 +500,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) attn_chunked_tc_kernel(const __
 #pragma unroll
       for (int e = 0; e < 8; ++e) mx[e] = -INFINITY;
       if (uni) {
+        const float2 lt2 = make_float2(ltau, ltau);
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          s[j] *= ltau;
-          mx[(j >> 4) * 4 + (j & 3)] = fmaxf(mx[(j >> 4) * 4 + (j & 3)], s[j]);
+        for (int j = 0; j < 32; j += 2) {
+          const float2 z = mul2(make_float2(s[j], s[j + 1]), lt2);
+          s[j] = z.x;
+          s[j + 1] = z.y;
+          mx[(j >> 4) * 4 + (j & 3)] = fmaxf(mx[(j >> 4) * 4 + (j & 3)], z.x);
+          mx[(j >> 4) * 4 + ((j + 1) & 3)] = fmaxf(mx[(j >> 4) * 4 + ((j + 1) & 3)], z.y);
         }
       } else {
 #pragma unroll
@@ -538,28 +563,43 @@ __global__ void __launch_bounds__(kWsThreads, 1) attn_chunked_tc_kernel(const __
       // P of the two heads (f16, times the window rows' scales) into the A operand; the row
       // sums add the unrounded values
       uint8_t *ps = s_dyn + kOffP + x * kPBytes;
-      float p[32];
+      float2 la[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f),
+                      make_float2(0.f, 0.f)};                // partial sums [head][parity of g], per pair
+      const float2 m0p = make_float2(m0, m0), m1p = make_float2(m1, m1);
+      if (uni) {
 #pragma unroll
-      for (int j = 0; j < 32; ++j) {
-        const float mh = j < 16 ? m0 : m1;
-        p[j] = (uni || s[j] != -INFINITY) ? ex2_approx(s[j] - mh) : 0.f;
-      }
-      float la[4] = {0.f, 0.f, 0.f, 0.f};                    // partial sums [head][parity of g]
+        for (int g = 0; g < 8; ++g) {
 #pragma unroll
-      for (int j = 0; j < 32; j += 2) la[(j >> 4) * 2 + ((j >> 1) & 1)] += p[j] + p[j + 1];
-#pragma unroll
-      for (int g = 0; g < 8; ++g) {
-        float2 v = make_float2(1.f, 1.f);
-        if (!uni) {
-          v = *reinterpret_cast<const float2 *>(kv + 8 * g + 2 * q4);
-          v.x = fmaxf(v.x, 0.f);
-          v.y = fmaxf(v.y, 0.f);
+          for (int hh = 0; hh < 2; ++hh) {
+            const int j = 16 * hh + 2 * g;
+            const float2 d = sub2(make_float2(s[j], s[j + 1]), hh ? m1p : m0p);
+            const float2 pp = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+            la[2 * hh + (g & 1)] = add2(la[2 * hh + (g & 1)], pp);
+            *reinterpret_cast<uint32_t *>(ps + (hh ? p1off : p0off) + g * 128) = pack_f16x2(pp.x, pp.y);
+          }
         }
-        *reinterpret_cast<uint32_t *>(ps + p0off + g * 128) = pack_f16x2(p[2 * g] * v.x, p[2 * g + 1] * v.y);
-        *reinterpret_cast<uint32_t *>(ps + p1off + g * 128) = pack_f16x2(p[16 + 2 * g] * v.x, p[16 + 2 * g + 1] * v.y);
+      } else {
+#pragma unroll
+        for (int g = 0; g < 8; ++g) {
+          const float2 v = *reinterpret_cast<const float2 *>(kv + 8 * g + 2 * q4);
+          const float2 vv = make_float2(fmaxf(v.x, 0.f), fmaxf(v.y, 0.f));
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            const int j = 16 * hh + 2 * g;
+            const float2 d = sub2(make_float2(s[j], s[j + 1]), hh ? m1p : m0p);
+            const float2 pp = make_float2(s[j] == -INFINITY ? 0.f : ex2_approx(d.x),
+                                          s[j + 1] == -INFINITY ? 0.f : ex2_approx(d.y));
+            la[2 * hh + (g & 1)] = add2(la[2 * hh + (g & 1)], pp);
+            const float2 pv = mul2(pp, vv);
+            *reinterpret_cast<uint32_t *>(ps + (hh ? p1off : p0off) + g * 128) = pack_f16x2(pv.x, pv.y);
+          }
+        }
       }
-      l0 = l0 * al0 + (la[0] + la[1]);
-      l1 = l1 * al1 + (la[2] + la[3]);
+      {
+        const float2 s0 = add2(la[0], la[1]), s1 = add2(la[2], la[3]);
+        l0 = l0 * al0 + (s0.x + s0.y);
+        l1 = l1 * al1 + (s1.x + s1.y);
+      }
       // a head's reference maximum rose: rescale this warp's half of its O row once the P V
       // of step u - 1 is in (the TMEM access is warp-wide, so the warp rescales when any of
       // its heads needs it)

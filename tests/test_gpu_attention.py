@@ -257,3 +257,14 @@ def test_tensor_core_path_interleaved_sessions():
     topk = synth.causal_topk(13, q_pos, 512)
     e = _check(w, _queries(T, 64, layer=9), q_seq, q_pos, topk, 128, LSE_TOL_TC)
     print(f"max rel err {e:.3e}")
+
+
+def test_tensor_core_path_single_chunk_rows():
+    # one step per row (top-k of at most 128, no window): row ends follow each other at every
+    # step, so each row's read-out and the next rows' products interleave most tightly
+    L = 3000
+    w = World([L], ring=128)
+    q_pos = np.arange(L - 300, L, dtype=np.int64)
+    topk = synth.causal_topk(14, q_pos, 96)
+    e = _check(w, _queries(300, 64, layer=10), np.zeros(300, np.int32), q_pos, topk, 0, LSE_TOL_TC)
+    print(f"max rel err {e:.3e}")
