@@ -45,9 +45,10 @@ SCAN_SCORE_STORE = 4             # the scan's own per-position score store (scra
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one scan launch, from one ncu
 # capture of the decode batch, valid only while the scan's sources are the ones captured: the
 # digest covers them, and any change reports the traffic as null.
-SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142737664 + 6975232}
-SCAN_NCU_SOURCES = ("sparse_attention_fp4_02_b300/csrc/indexer.cu", "sparse_attention_fp4_02_b300/csrc/common.cuh")
-SCAN_NCU_DIGEST = "a50fb76dda3dc0b46311a0e21954d99404226223c9558bec7bdd17ba9f524e1a"
+SCAN_NCU_TRAFFIC = {"decode_b32_ctx65536_full+3reuse": 142743808 + 5939200}
+SCAN_NCU_SOURCES = ("sparse_attention_fp4_02_b300/csrc/indexer.cu", "sparse_attention_fp4_02_b300/csrc/common.cuh",
+                    "sparse_attention_fp4_02_b300/csrc/tcgen05.cuh")
+SCAN_NCU_DIGEST = "ea28df0a1d0319d4b3aa4b6446d84560e480f45cb6d2f3b6ebe86e79df77c1eb"
 
 
 def scan_traffic(workload: str):
