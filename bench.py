@@ -192,7 +192,7 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
     scan's own launch time from events recorded inside the graph on its stream, the same step
     end to end with host copies, and optionally a per-call breakdown."""
     import torch
-    from sparse_attention_fp4_02_b300.runner import DecodeRunner
+    from sparse_attention_fp4_02_b300.runner import DecodeRunner, StepPipeline
     from synth.workloads import config
 
     wl = config(cfg) if isinstance(cfg, int) else cfg
@@ -217,7 +217,6 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
     with torch.cuda.graph(g):
         for i in range(G):
             r.step(prof=ev[i])
-    g1 = r.capture()
     for _ in range(max(1, math.ceil(warmup / G))):
         g.replay()
     barrier(world)
@@ -232,35 +231,37 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
     r.check_device_errors()
     ms = max_over_ranks(ms, world)
 
-    # end to end through the public API with host buffers: pinned inputs in, outputs out, every step
+    # end to end through the public API with host buffers: every step copies its inputs in from
+    # pinned host memory and its outputs back, on copy streams that overlap the neighbouring
+    # steps' compute (runner.StepPipeline: two alternating sets of step buffers)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_in = [(pin(r.h_kv_new.view(np.int16)), r.kv_new), (pin(r.h_ik_new.view(np.int16)), r.ik_new),
-            (pin(r.h_swa_new.view(np.int16)), r.swa_new), (pin(r.h_q.view(np.int16)), r.q)]
-    h_in += [(pin(r.h_qidx[l].view(np.int16)), r.qidx[l]) for l in r.idx_layers]
-    h_in += [(pin(r.h_w[l]), r.w[l]) for l in r.idx_layers]
+    h_in = {"kv_new": pin(r.h_kv_new.view(np.int16)), "ik_new": pin(r.h_ik_new.view(np.int16)),
+            "swa_new": pin(r.h_swa_new.view(np.int16)), "q": pin(r.h_q.view(np.int16))}
+    for l in r.idx_layers:
+        h_in[f"qidx{l}"] = pin(r.h_qidx[l].view(np.int16))
+        h_in[f"w{l}"] = pin(r.h_w[l])
     if r.D > 1:                  # the Full layer's own copy of each session's last row
-        h_in += [(pin(r.h_qidx[l][r.D - 1::r.D].view(np.int16)), r.qidx_last[l]) for l in r.full_layers]
-        h_in += [(pin(r.h_w[l][r.D - 1::r.D]), r.w_last[l]) for l in r.full_layers]
-    h_out = [torch.empty(r.out.shape, dtype=torch.float32).pin_memory(),
-             torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()]
-    h2d = sum(h.numel() * h.element_size() for h, _ in h_in)
-    d2h = sum(h.numel() * h.element_size() for h in h_out)
+        for l in r.full_layers:
+            h_in[f"qidx_last{l}"] = pin(r.h_qidx[l][r.D - 1::r.D].view(np.int16))
+            h_in[f"w_last{l}"] = pin(r.h_w[l][r.D - 1::r.D])
+    h_out = {"out": torch.empty(r.out.shape, dtype=torch.float32).pin_memory(),
+             "lse": torch.empty(r.lse.shape, dtype=torch.float32).pin_memory()}
+    h2d = sum(h.numel() * h.element_size() for h in h_in.values())
+    d2h = sum(h.numel() * h.element_size() for h in h_out.values())
     n_e2e = min(steps, 2000)
+    pipe = StepPipeline(r)
 
-    def e2e_step():
-        for h, d in h_in:
-            d.view(torch.int16 if d.dtype == torch.bfloat16 else d.dtype).copy_(h, non_blocking=True)
-        g1.replay()
-        h_out[0].copy_(r.out, non_blocking=True)
-        h_out[1].copy_(r.lse, non_blocking=True)
-
+    pipe.begin()
     for _ in range(3):
-        e2e_step()
+        pipe.step(h_in, h_out)
+    pipe.end()
     barrier(world)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record()
+    pipe.begin()
     for _ in range(n_e2e):
-        e2e_step()
+        pipe.step(h_in, h_out)
+    pipe.end()
     e1.record()
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
@@ -277,7 +278,7 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
         "launches": kernels_per_step(wl) * steps,
         "rows_per_step": r.T,
     }
-    del g, g1
+    del g, pipe
     if breakdown:
         res["breakdown_us"] = measure_breakdown(r)
     del r

@@ -211,6 +211,31 @@ class DecodeRunner:
         if v:
             raise RuntimeError(f"device error bits 0x{v:x}")
 
+    def step_buffers(self) -> dict:
+        """The step's own device inputs and outputs by name: the tensors a step reads and writes
+        besides the cache, the SWA rings and the selection scratch."""
+        b = {"kv_new": self.kv_new, "ik_new": self.ik_new, "swa_new": self.swa_new, "q": self.q,
+             "out": self.out, "lse": self.lse}
+        for l in self.idx_layers:
+            b[f"qidx{l}"] = self.qidx[l]
+            b[f"w{l}"] = self.w[l]
+        if self.D > 1:
+            for l in self.full_layers:
+                b[f"qidx_last{l}"] = self.qidx_last[l]
+                b[f"w_last{l}"] = self.w_last[l]
+        return b
+
+    def use_buffers(self, b: dict):
+        """Make later steps (and captures) read and write the given set of step buffers."""
+        self.kv_new, self.ik_new, self.swa_new, self.q = b["kv_new"], b["ik_new"], b["swa_new"], b["q"]
+        self.out, self.lse = b["out"], b["lse"]
+        for l in self.idx_layers:
+            self.qidx[l] = b[f"qidx{l}"]
+            self.w[l] = b[f"w{l}"]
+        for l in self.full_layers:
+            self.qidx_last[l] = b[f"qidx_last{l}"] if self.D > 1 else self.qidx[l]
+            self.w_last[l] = b[f"w_last{l}"] if self.D > 1 else self.w[l]
+
     def capture(self, prof=None):
         """Capture one step into a CUDA graph; returns the graph (replay with .replay())."""
         s = torch.cuda.Stream()
@@ -323,3 +348,63 @@ class ChunkedRunner:
         v = int(self.d_err.item())
         if v:
             raise RuntimeError(f"device error bits 0x{v:x}")
+
+
+class StepPipeline:
+    """Decode steps served from host memory: every step's inputs are copied in from pinned
+    host buffers and its outputs copied back, on copy streams of their own, so that the
+    copies overlap the neighbouring steps' compute.  Two sets of device inputs and outputs
+    alternate, each with its own captured step graph: step k's inputs go into set k % 2
+    once step k - 2 has finished with it, step k computes once its inputs are in and step
+    k - 2's outputs have been read back, and step k's outputs are read back while step k + 1
+    computes.  The steps themselves run in order on the current stream (they share the
+    cache and the selection scratch)."""
+
+    def __init__(self, runner: DecodeRunner):
+        self.r = runner
+        base = runner.step_buffers()
+        alt = {k: v.clone() for k, v in base.items()}
+        self.sets = [base, alt]
+        self.graphs = []
+        for b in self.sets:
+            runner.use_buffers(b)
+            self.graphs.append(runner.capture())
+        runner.use_buffers(base)
+        self.s_in, self.s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        self.in_ready = [torch.cuda.Event() for _ in range(2)]
+        self.done = [torch.cuda.Event() for _ in range(2)]
+        self.out_done = [torch.cuda.Event() for _ in range(2)]
+        self.k = 0
+
+    def begin(self):
+        """Order the copy streams after the work already on the current stream."""
+        cur = torch.cuda.current_stream()
+        self.s_in.wait_stream(cur)
+        self.s_out.wait_stream(cur)
+
+    def step(self, h_in: dict, h_out: dict):
+        """Enqueue one step: h_in maps input names (see DecodeRunner.step_buffers) to pinned
+        host tensors, h_out maps "out" / "lse" to pinned host tensors that receive them."""
+        x = self.k & 1
+        dev = self.sets[x]
+        cur = torch.cuda.current_stream()
+        with torch.cuda.stream(self.s_in):
+            self.s_in.wait_event(self.done[x])          # step k - 2 has read this set's inputs
+            for name, h in h_in.items():
+                d = dev[name]
+                (d.view(torch.int16) if d.dtype == torch.bfloat16 else d).copy_(h, non_blocking=True)
+            self.in_ready[x].record(self.s_in)
+        cur.wait_event(self.in_ready[x])
+        cur.wait_event(self.out_done[x])                # step k - 2's outputs have been read back
+        self.graphs[x].replay()
+        self.done[x].record(cur)
+        with torch.cuda.stream(self.s_out):
+            self.s_out.wait_event(self.done[x])
+            for name, h in h_out.items():
+                h.copy_(dev[name], non_blocking=True)
+            self.out_done[x].record(self.s_out)
+        self.k += 1
+
+    def end(self):
+        """Order the current stream after every copy back issued so far."""
+        torch.cuda.current_stream().wait_stream(self.s_out)
