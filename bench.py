@@ -271,6 +271,28 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     r.check_device_errors()
+    # the same copies on the compute stream, one step after another: a single batch whose
+    # next inputs depend on its own last outputs cannot overlap them
+    dev0 = pipe.sets[0]
+
+    def serial_step():
+        for name, h in h_in.items():
+            d = dev0[name]
+            (d.view(torch.int16) if d.dtype == torch.bfloat16 else d).copy_(h, non_blocking=True)
+        pipe.graphs[0].replay()
+        for name, h in h_out.items():
+            h.copy_(dev0[name], non_blocking=True)
+
+    for _ in range(3):
+        serial_step()
+    barrier(world)
+    e0.record()
+    for _ in range(n_e2e):
+        serial_step()
+    e1.record()
+    barrier(world)
+    serial_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    r.check_device_errors()
 
     parts = r.step_bytes()
     res = {
@@ -279,7 +301,9 @@ def measure_workload(cfg, steps: int, warmup: int, world: int, graph_steps: int 
         "scan_bytes": SCAN_BYTES_PER_POS * int(wl.lengths.sum()),
         "step_bytes": parts, "step_bytes_total": int(sum(parts.values())),
         "e2e": {"value": aggregate_rate(r.T * n_e2e, world, e2e_ms), "unit": "query-steps/s",
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e},
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "steps": n_e2e,
+                "overlap": "two alternating step-buffer sets (two independent batches in flight)",
+                "serial": aggregate_rate(r.T * n_e2e, world, serial_ms)},
         "launches": kernels_per_step(wl) * steps,
         "rows_per_step": r.T,
     }
@@ -455,7 +479,8 @@ def workload_line(res, peak):
             "scan_us": res["scan_ms"] * 1e3, "scan_gbs": a, "scan_frac": a / peak, "scan_frac_nominal": a / NOMINAL_HBM_GBS,
             "step_bytes": res["step_bytes"], "step_gbs": step_gbs, "step_frac": step_gbs / peak,
             "step_frac_nominal": step_gbs / NOMINAL_HBM_GBS,
-            "e2e": res["e2e"]["value"], "h2d_bytes_per_step": res["e2e"]["h2d_bytes_per_step"],
+            "e2e": res["e2e"]["value"], "e2e_serial": res["e2e"]["serial"],
+            "h2d_bytes_per_step": res["e2e"]["h2d_bytes_per_step"],
             "d2h_bytes_per_step": res["e2e"]["d2h_bytes_per_step"], "gpu_launches": res["launches"],
             "breakdown_us": res.get("breakdown_us")}
 
