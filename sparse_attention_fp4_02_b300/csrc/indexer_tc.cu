@@ -187,7 +187,9 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
         float o = acc * pend_ks;
         o = o > 0.f ? o : 0.f;                                // also maps NaN and -0 to +0
         const bool valid = kk < s_len[jr];
-        if (valid) a.ws.sigma[((int64_t)cur_g * kCqRows + jr) * a.ws.sigma_stride + kk] = o;
+        // streaming store (evict first): 4 bytes per (row, position), read back only for the
+        // candidate blocks, so the keys of the group stay in L2
+        if (valid) __stcs(a.ws.sigma + ((int64_t)cur_g * kCqRows + jr) * a.ws.sigma_stride + kk, o);
         smx[4 * pass + j] = fmaxf(smx[4 * pass + j], valid ? pend_ks : 0.f);
         float m = valid ? o : 0.f;
 #pragma unroll
