@@ -17,6 +17,7 @@
 // MMAs into one of two TMEM accumulators, and the epilogue of the previous tile runs while
 // the tensor cores work on the current one.
 #include <cfloat>
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -42,6 +43,16 @@ static_assert(kCqN == 256, "one accumulator is 256 columns");
 // Byte offset of (row n, dims 8kg..8kg+7) in a K-major no-swizzle operand of 64 dims.
 __device__ __forceinline__ int cq_off(int n, int kg) { return (n >> 3) * kCqRowGroupBytes + kg * 128 + (n & 7) * 16; }
 
+// d = a * b + c on two float32 lanes at once, each rounded to nearest
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  const uint64_t ab = ((uint64_t)__float_as_uint(a.y) << 32) | __float_as_uint(a.x);
+  const uint64_t bb = ((uint64_t)__float_as_uint(b.y) << 32) | __float_as_uint(b.x);
+  const uint64_t cb = ((uint64_t)__float_as_uint(c.y) << 32) | __float_as_uint(c.x);
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;\n" : "=l"(r) : "l"(ab), "l"(bb), "l"(cb));
+  return make_float2(__uint_as_float((uint32_t)r), __uint_as_float((uint32_t)(r >> 32)));
+}
+
 // A group of rows is scored here when all its rows share one session (one base).
 __device__ __forceinline__ bool cq_uniform(const CqArgs &a, int g, int64_t &base, int32_t &maxlen) {
   const int r0 = g * kCqRows, r1 = min(a.n, r0 + kCqRows);
@@ -64,7 +75,7 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
   __shared__ int64_t s_base[kCqMaxGroups];
   __shared__ int32_t s_maxlen[kCqMaxGroups];
   __shared__ __align__(16) float s_wi[kCqRows][kHIdx];       // w * 2^-c of the current group
-  __shared__ int32_t s_len[kCqRows];                          // lengths of the current group's rows
+  __shared__ __align__(16) int32_t s_len[kCqRows];            // lengths of the current group's rows
   pdl_enter();
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int ngroups = (a.n + kCqRows - 1) / kCqRows;
@@ -139,18 +150,20 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
   };
 
   // the current group's rows of this thread (8 eq .. 8 eq + 7): largest valid key scale seen
-  float smx[8];
+  // (smx_all: the same for every row, from the tiles that all eight rows cover)
+  float smx[8], smx_all = 0.f;
 #pragma unroll
   for (int j = 0; j < 8; ++j) smx[j] = 0.f;
   int cur_g = -1;
   auto flush_smax = [&]() {
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      const float m = warp_max(smx[j]);
+      const float m = warp_max(fmaxf(smx[j], smx_all));
       const int r = cur_g * kCqRows + 8 * eq + j;
       if (lane == 0 && r < a.n && m > 0.f) atomicMax(&a.ws.smax[r], __float_as_uint(m));
       smx[j] = 0.f;
     }
+    smx_all = 0.f;
   };
 
   uint32_t ph0 = 0, ph1 = 0;
@@ -169,54 +182,78 @@ __global__ void __launch_bounds__(kCqThreads, 1) chunk_scores_tc_kernel(const __
     if (!ok) { dead = true; if (lane == 0) set_err(a.d_err, CSA2_DEVERR_TIMEOUT); return; }
     const int em = 32 * (warp & 3) + lane;                    // == km
     const int kk = (int)pend_tile * kCqKeys + em;             // < 2^31: positions of one row
+    // the warp's eight rows all reach past the tile's last key (the usual case): no
+    // per-position validity (warp-uniform, as eq is)
+    const int4 la = *reinterpret_cast<const int4 *>(&s_len[8 * eq]);
+    const int4 lb = *reinterpret_cast<const int4 *>(&s_len[8 * eq + 4]);
+    const int minlen = min(min(min(la.x, la.y), min(la.z, la.w)), min(min(lb.x, lb.y), min(lb.z, lb.w)));
+    const bool full = (int)pend_tile * kCqKeys + kCqKeys <= minlen;
+    float *sig = a.ws.sigma + ((int64_t)cur_g * kCqRows + 8 * eq) * a.ws.sigma_stride + kk;
+    const int64_t sst = a.ws.sigma_stride;
+    float blk[8];                                             // row j's score, 0 where not valid
+    auto rows = [&](auto full_t) {
+      constexpr bool kFull = decltype(full_t)::value;
 #pragma unroll
-    for (int pass = 0; pass < 2; ++pass) {                    // rows 8 eq + 4 pass + j
-      float v[32];
-      tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eq + 32 * pass, v);
-      float bm[4];
-      bool bv[4];
+      for (int pass = 0; pass < 2; ++pass) {                  // rows 8 eq + 4 pass + j
+        float v[32];
+        tmem_ld32(tmem + lane_off + pend_buf * kCqN + 64 * eq + 32 * pass, v);
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int jr = 8 * eq + 4 * pass + j;
-        const float4 w0 = *reinterpret_cast<const float4 *>(&s_wi[jr][0]);
-        const float4 w1 = *reinterpret_cast<const float4 *>(&s_wi[jr][4]);
-        const float wv[kHIdx] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
-        float acc = 0.f;
-#pragma unroll
-        for (int h = 0; h < kHIdx; ++h) acc = fmaf(fmaxf(v[8 * j + h], 0.f), wv[h], acc);
-        float o = acc * pend_ks;
-        o = o > 0.f ? o : 0.f;                                // also maps NaN and -0 to +0
-        const bool valid = kk < s_len[jr];
-        // streaming store (evict first): 4 bytes per (row, position), read back only for the
-        // candidate blocks, so the keys of the group stay in L2
-        if (valid) __stcs(a.ws.sigma + ((int64_t)cur_g * kCqRows + jr) * a.ws.sigma_stride + kk, o);
-        smx[4 * pass + j] = fmaxf(smx[4 * pass + j], valid ? pend_ks : 0.f);
-        float m = valid ? o : 0.f;
-#pragma unroll
-        for (int s = 1; s < BLOCK; s <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, s));
-        bm[j] = m;                                            // the block's maximum, in every lane of it
-        bv[j] = __shfl_sync(0xffffffffu, valid, lane & ~(BLOCK - 1));   // its first position is valid
-      }
-      // lane i of a block writes row i's maximum (BLOCK >= 4), or the block's first lane all four
-      if (BLOCK >= 4) {
-        const int jj = em & (BLOCK - 1);
-        if (jj < 4) {
-          const float m = jj == 0 ? bm[0] : jj == 1 ? bm[1] : jj == 2 ? bm[2] : bm[3];
-          const bool ok = jj == 0 ? bv[0] : jj == 1 ? bv[1] : jj == 2 ? bv[2] : bv[3];
-          if (ok) {
-            const int64_t r = (int64_t)cur_g * kCqRows + 8 * eq + 4 * pass + jj;
-            a.ws.bmax[r * a.ws.nbm + (kk - jj) / BLOCK] = m;
-            atomicAdd(&a.ws.hist[r * kHistBins + min(__float_as_uint(m) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
-          }
+        for (int j = 0; j < 4; ++j) {
+          const int jj = 4 * pass + j, jr = 8 * eq + jj;
+          const float4 w0 = *reinterpret_cast<const float4 *>(&s_wi[jr][0]);
+          const float4 w1 = *reinterpret_cast<const float4 *>(&s_wi[jr][4]);
+          // sum_h w_h max(v_h, 0) as two interleaved chains of four (w >= 0: every term is
+          // non-negative, so each result keeps at most five roundings of the sum)
+          float2 acc = fma2(make_float2(fmaxf(v[8 * j], 0.f), fmaxf(v[8 * j + 1], 0.f)), make_float2(w0.x, w0.y),
+                            make_float2(0.f, 0.f));
+          acc = fma2(make_float2(fmaxf(v[8 * j + 2], 0.f), fmaxf(v[8 * j + 3], 0.f)), make_float2(w0.z, w0.w), acc);
+          acc = fma2(make_float2(fmaxf(v[8 * j + 4], 0.f), fmaxf(v[8 * j + 5], 0.f)), make_float2(w1.x, w1.y), acc);
+          acc = fma2(make_float2(fmaxf(v[8 * j + 6], 0.f), fmaxf(v[8 * j + 7], 0.f)), make_float2(w1.z, w1.w), acc);
+          float o = (acc.x + acc.y) * pend_ks;
+          o = o > 0.f ? o : 0.f;                              // also maps NaN and -0 to +0
+          const bool valid = kFull || kk < s_len[jr];
+          // streaming store (evict first): 4 bytes per (row, position), read back only for
+          // the candidate blocks, so the keys of the group stay in L2
+          if (valid) __stcs(sig + jj * sst, o);
+          if (!kFull) smx[jj] = fmaxf(smx[jj], valid ? pend_ks : 0.f);
+          blk[jj] = valid ? o : 0.f;
         }
-      } else {
+      }
+    };
+    if (full) { rows(std::true_type{}); smx_all = fmaxf(smx_all, pend_ks); }
+    else rows(std::false_type{});
+
+    // Block maxima by a reduce-scatter over the lanes of each block: stage s halves the
+    // rows a lane holds, the lane with bit d = kBl / 2^(s+1) set keeping the upper half, so
+    // lane i of a block (i < kBl) ends with the maxima of rows kNb i .. kNb i + kNb - 1.
+    constexpr int kBl = BLOCK < 8 ? BLOCK : 8;
+    constexpr int kNb = 8 / kBl;
+    constexpr int kStages = kBl == 8 ? 3 : kBl == 4 ? 2 : kBl == 2 ? 1 : 0;
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          if ((em % BLOCK) == 0 && bv[j]) {
-            const int64_t r = (int64_t)cur_g * kCqRows + 8 * eq + 4 * pass + j;
-            a.ws.bmax[r * a.ws.nbm + kk / BLOCK] = bm[j];
-            atomicAdd(&a.ws.hist[r * kHistBins + min(__float_as_uint(bm[j]) >> kHistShift, (uint32_t)kHistBins - 1)], 1u);
-          }
+    for (int st = 0; st < kStages; ++st) {
+      const int d = kBl >> (st + 1), half = 4 >> st;
+      const bool up = (lane & d) != 0;
+#pragma unroll
+      for (int i = 0; i < half; ++i) {
+        const float keep = up ? blk[half + i] : blk[i];
+        const float send = up ? blk[i] : blk[half + i];
+        blk[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, d));
+      }
+    }
+#pragma unroll
+    for (int d = 8; d < BLOCK; d <<= 1) blk[0] = fmaxf(blk[0], __shfl_xor_sync(0xffffffffu, blk[0], d));
+    // a block is recorded when its first position is valid for the row
+    if ((em & (BLOCK - 1)) < kBl) {
+      const int kb0 = kk & ~(BLOCK - 1);
+#pragma unroll
+      for (int i = 0; i < kNb; ++i) {
+        const int jr = 8 * eq + (em & (kBl - 1)) * kNb + i;
+        if (kb0 < s_len[jr]) {
+          const int64_t r = (int64_t)cur_g * kCqRows + jr;
+          a.ws.bmax[r * a.ws.nbm + kk / BLOCK] = blk[i];
+          atomicAdd(&a.ws.hist[r * kHistBins + min(__float_as_uint(blk[i]) >> kHistShift, (uint32_t)kHistBins - 1)],
+                    1u);
+        }
       }
     }
   };
