@@ -8,9 +8,12 @@
 // The E4M3 keys are converted exactly to f16 into shared-memory core matrices, the queries
 // are scaled per (row, head) by the same power of two as in the one-query scan (so the same
 // certified error bound holds), D accumulates in TMEM, and the epilogue (thread <-> key,
-// eight rows per thread in two passes of four) forms ReLU * w, the key scale, the block maxima and their
-// histogram, and stores every position's score for the exact selection that follows.
-// A row only counts the positions up to its own (its length in the row view).
+// eight rows per thread in two passes of four) forms ReLU * w summed over the heads with
+// packed f32x2 FMAs, applies the key scale, stores every position's score for the exact
+// selection that follows, and takes the block maxima by a reduce-scatter across the lanes
+// of each block (each lane ends with whole rows' maxima) for their histogram.  A row only
+// counts the positions up to its own (its length in the row view); tiles that every row of
+// a warp reaches past skip the per-position checks.
 //
 // Pipeline per CTA (persistent over (group, tile) items): the raw bytes of the next tile
 // are loaded into registers while the current tile is converted, one thread issues the
