@@ -62,10 +62,18 @@ def test_decoder_sizes_rows_near_the_end():
     assert compare([L], np.zeros(q_pos.shape[0], np.int32), q_pos) == 0
 
 
-@pytest.mark.parametrize("block,n_keep,topk", [(1, 64, 64), (4, 100, 17), (16, 40, 40)])
+@pytest.mark.parametrize("block,n_keep,topk", [(1, 64, 64), (2, 30, 9), (4, 100, 17), (16, 40, 40)])
 def test_other_block_pool_topk_sizes(block, n_keep, topk):
     q_pos = np.array([0, 63, 700, 2222, 4999], np.int64)
     assert compare([5000], np.zeros(5, np.int32), q_pos, block, n_keep, topk) == 0
+
+
+@pytest.mark.parametrize("block,n_keep,topk", [(1, 64, 64), (2, 300, 50), (4, 100, 17), (16, 40, 40)])
+def test_other_block_sizes_on_whole_tiles(block, n_keep, topk):
+    # 40 rows near the end of one session: the first group's rows all reach past most key
+    # tiles (the scores' whole-tile path), the second group is mostly empty rows
+    q_pos = np.arange(4960, 5000, dtype=np.int64)
+    assert compare([5000], np.zeros(40, np.int32), q_pos, block, n_keep, topk) == 0
 
 
 def test_more_rows_than_one_group():
