@@ -108,6 +108,13 @@ def test_row_mode_workspace_sizes(lib):
     assert f(*args(5, 262144, 8, 2048, 512, 1024)) == 0 and out.value < c4096
     assert f(*args(5, 262144, 8, 2048, 512, (1 << 24) + 1)) == 1
     assert f(*args(5, 262144, 5, 2048, 512, 16)) == 1      # block not a power of two
+    # every supported block size; fewer, larger blocks never need more workspace
+    sizes = []
+    for blk in (1, 2, 4, 8, 16):
+        assert f(*args(5, 262144, blk, 2048, 512, 1024)) == 0
+        sizes.append(out.value)
+    assert sizes == sorted(sizes, reverse=True) and sizes[0] > sizes[-1]
+    assert f(*args(5, 262144, 32, 2048, 512, 1024)) == 1   # block beyond 16
 
 
 def test_row_mode_entry_points_reject_bad_arguments_without_a_gpu(lib):
